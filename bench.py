@@ -1,0 +1,350 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused GEMM + bias + ReLU (C = relu(A.B + bias)) on GB300.
+
+One step = one fused GEMM launch over the workload's synthetic inputs, already
+resident in HBM.  Prints ONE JSON line (rank 0):
+
+  value        TFLOP/s = 2MNK / (mean device time of the step), summed over ranks
+  e2e          the same through tgemm_run_host: host buffers (pinned), host->device
+               copies, the GEMM and the device->host copy of C inside the timed region
+  roofline     the fused kernel's achieved TFLOP/s (algorithmic 2MNK per launch over
+               the CUDA-event launch time) against the measured dense bf16 peak
+  cpu_baseline the fp64 CPU oracle on a bounded sample of rows of the same workload
+  clocks       SM clocks and throttle reasons sampled during the timed region
+
+--impl reference times the CPU oracle itself as the reference arm.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (weak
+scaling, no collective on the data path); the timed region is bracketed by a
+barrier and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "fused GEMM+bias+ReLU TFLOP/s (2MNK/t) on 1 GB300; % of dense fp16 tensor peak"
+DEFAULT_WORKLOAD = "c1"
+FLUSH_BYTES = 256 << 20            # > 2x the 129 MB L2
+KERNEL_SOURCES = ["gemm_epilogue_02_gb300/csrc/gemm_kernel.cuh", "gemm_epilogue_02_gb300/csrc/ptx.cuh",
+                  "gemm_epilogue_02_gb300/csrc/tgemm_api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 6800.0, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_hash") == kernel_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(w, target_s: float):
+    """Time the fp64 oracle (as it stands) on a bounded sample of rows."""
+    import oracle
+    A, B, bias = si.make_workload(w)
+    ba, bb = si.bits(A), si.bits(B)
+    bc = si.bits(bias) if bias is not None else None
+    epi = si.EPILOGUES[w.epilogue]
+    dt = oracle.dtype_code(w.dtype)
+    cores = oracle.max_threads()
+    probe = list(range(min(w.M, max(cores, 1))))
+    t0 = time.perf_counter()
+    oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=probe)
+    t_probe = time.perf_counter() - t0
+    rows_n = int(max(len(probe), min(w.M, len(probe) * target_s / max(t_probe, 1e-6))))
+    rows = list(range(rows_n))
+    t0 = time.perf_counter()
+    oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=rows)
+    t = time.perf_counter() - t0
+    return {"value": 2.0 * rows_n * w.N * w.K / t / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "seconds": round(t, 3),
+            "sample": f"first {rows_n} of {w.M} rows of {w.name} (all {w.N} columns, K={w.K}), fp64"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU oracle on a bounded sample per step (rank 0 only)."""
+    if rank != 0:
+        return 0
+    import oracle
+    w = si.WORKLOADS[args.config]
+    A, B, bias = si.make_workload(w)
+    ba, bb = si.bits(A), si.bits(B)
+    bc = si.bits(bias) if bias is not None else None
+    epi = si.EPILOGUES[w.epilogue]
+    dt = oracle.dtype_code(w.dtype)
+    cores = oracle.max_threads()
+    rows = list(range(min(w.M, args.ref_rows)))
+    for _ in range(args.warmup):
+        oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=rows)
+        times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    value = 2.0 * len(rows) * w.N * w.K / t / 1e12
+    sample = f"first {len(rows)} of {w.M} rows of {w.name} per step (all {w.N} columns, K={w.K}), fp64"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype,
+            "epilogue": w.epilogue, "lda": w.lda or w.K, "ldb": w.ldb or w.N, "ldc": w.ldc or w.N,
+            "inputs": "A~N(0,1), B~N(0,1)/sqrt(K), bias~N(0,0.1)" if w.kind == "normal"
+            else "uniform integers in {-2..2}", "seed": w.seed,
+            "l2": "flushed between steps (256 MiB write, outside the timed launch)"}
+
+
+def run_tgemm_bench(args, world, rank, local):
+    import gemm_epilogue_02_gb300 as tg
+    tg.load()
+    w = si.WORKLOADS[args.config]
+    dev = torch.device("cuda", local)
+    A, B, bias = si.make_workload(w)
+    ldc = w.ldc or w.N
+    Ad = A.to(dev)[:, : w.K]
+    Bd = B.to(dev)[:, : w.N]
+    bd = bias.to(dev) if bias is not None else None
+    Cfull = torch.empty((w.M, ldc), dtype=A.dtype, device=dev)
+    Cd = Cfull[:, : w.N]
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    flops = float(w.flops)
+
+    def step():
+        tg.run(Ad, Bd, bd, Cd, w.epilogue, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize(dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        with ClockSampler(local) as clk:
+            t_wall = time.perf_counter()
+            for i in range(args.steps):
+                flush.zero_()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            torch.cuda.synchronize(dev)
+            t_wall = time.perf_counter() - t_wall
+        barrier(world)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_ms = sum(launch_ms) / len(launch_ms)
+    mean_ms_max = max_over_ranks(mean_ms, world)
+    value = world * flops / (mean_ms_max * 1e-3) / 1e12
+
+    # End to end through the host-buffer entry point (pinned host memory).
+    e2e = None
+    if not args.no_e2e:
+        Ah, Bh = A.pin_memory(), B.pin_memory()
+        bh = bias.pin_memory() if bias is not None else None
+        Ch = torch.empty((w.M, ldc), dtype=A.dtype).pin_memory()
+        Chv = Ch[:, : w.N]
+        Ahv, Bhv = Ah[:, : w.K], Bh[:, : w.N]
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup)):
+                tg.run_host(Ahv, Bhv, bh, Chv, w.epilogue, stream=stream, device=dev)
+            torch.cuda.synchronize(dev)
+            n_e2e = max(3, min(args.steps, 20))
+            es = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+            ee = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+            barrier(world)
+            for i in range(n_e2e):
+                es[i].record(stream)
+                tg.run_host(Ahv, Bhv, bh, Chv, w.epilogue, stream=stream, device=dev)
+                ee[i].record(stream)
+            torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(es, ee)) / n_e2e, world)
+        h2d = (w.M * w.K + w.K * w.N + (w.N if bias is not None else 0)) * 2
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": w.M * w.N * 2,
+               "ms_per_step": e2e_ms, "steps": n_e2e, "host_memory": "pinned"}
+
+    status = tg.tgemm_last_device_status()
+    if rank != 0:
+        return 0 if status == 0 else 1
+
+    peak, hbm, peak_kind = measured_peaks()
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    traffic = recorded_traffic(args.config)
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "config": workload_config(w),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} dense bf16 burst (fp16 nominal rate is equal)",
+                         "kernel": "tgemm_fused_kernel", "algorithmic_flops_per_launch": flops,
+                         "algorithmic_bytes_per_launch": (w.M * w.K + w.K * w.N + w.M * w.N + w.N) * 2},
+            "clocks": clk.summary(),
+            "gpu_launches": args.steps * (1 + (1 if (w.lda or w.K) % 8 else 0) + (1 if (w.ldb or w.N) % 8 else 0)),
+            "device_status": tg.tgemm_status_string(status),
+            "wall_s_timed_region": t_wall}
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0 if status == 0 else 1
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["tgemm", "reference"], default="tgemm")
+    ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-rows", type=int, default=64, help="oracle rows per reference step")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)          # at least 3 untimed warm-up steps
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+    else:
+        rc = run_tgemm_bench(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,75 @@
+"""Fused tensor-core GEMM epilogue for GB300 (sm_103a):  C = act(A.B + bias).
+
+The computation lives in the CUDA library (csrc/, C ABI in include/tgemm.h);
+this package only marshals torch tensors (device memory and the current
+stream) into that ABI.
+"""
+from __future__ import annotations
+
+import torch
+
+from ._binding import (  # noqa: F401
+    TGEMM_BF16, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_RELU, TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_F16,
+    EXPORTED, STATUS, TgemmError, library_path, load, tgemm_last_device_status, tgemm_run,
+    tgemm_run_host, tgemm_status_string, tgemm_version,
+)
+from .build import build  # noqa: F401
+
+EPILOGUES = {"none": TGEMM_EPI_NONE, "relu": TGEMM_EPI_RELU, "bias": TGEMM_EPI_BIAS,
+             "bias_relu": TGEMM_EPI_BIAS_RELU}
+_DT = {torch.float16: TGEMM_F16, torch.bfloat16: TGEMM_BF16}
+
+
+def _epi(epilogue) -> int:
+    return EPILOGUES[epilogue] if isinstance(epilogue, str) else int(epilogue)
+
+
+def _check_2d(name, t):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
+
+
+def run(A: torch.Tensor, B: torch.Tensor, bias, C: torch.Tensor, epilogue="bias_relu",
+        stream=None) -> torch.Tensor:
+    """C = epi(A @ B + bias) on CUDA tensors, enqueued on the current (or given) stream.
+
+    A [M, K], B [K, N], C [M, N] may have row pitches wider than their widths
+    (stride(0) >= width); bias is [N] or None.  Raises TgemmError on a status
+    other than TGEMM_OK.
+    """
+    _check_2d("A", A), _check_2d("B", B), _check_2d("C", C)
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
+    if not (A.dtype == B.dtype == C.dtype) or A.dtype not in _DT:
+        raise ValueError("A, B and C must share dtype float16 or bfloat16")
+    if bias is not None and (bias.dtype != A.dtype or bias.dim() != 1 or bias.numel() != N
+                             or bias.stride(0) != 1):
+        raise ValueError("bias must be a contiguous [N] tensor of the same dtype")
+    s = stream if stream is not None else torch.cuda.current_stream(A.device)
+    with torch.cuda.device(A.device):
+        st = tgemm_run(A.data_ptr(), B.data_ptr(), bias.data_ptr() if bias is not None else 0,
+                       C.data_ptr(), M, N, K, A.stride(0), B.stride(0), C.stride(0), _DT[A.dtype],
+                       _epi(epilogue), s.cuda_stream)
+    if st != 0:
+        raise TgemmError(st)
+    return C
+
+
+def run_host(A: torch.Tensor, B: torch.Tensor, bias, C: torch.Tensor, epilogue="bias_relu",
+             stream=None, device=None) -> torch.Tensor:
+    """The same on CPU tensors (ideally pinned): copies in, computes and copies C
+    back inside the library, on `stream` of `device`.  The caller synchronises."""
+    _check_2d("A", A), _check_2d("B", B), _check_2d("C", C)
+    M, K = A.shape
+    N = B.shape[1]
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = tgemm_run_host(A.data_ptr(), B.data_ptr(), bias.data_ptr() if bias is not None else 0,
+                            C.data_ptr(), M, N, K, A.stride(0), B.stride(0), C.stride(0),
+                            _DT[A.dtype], _epi(epilogue), s.cuda_stream)
+    if st != 0:
+        raise TgemmError(st, "tgemm_run_host")
+    return C

@@ -1,0 +1,86 @@
+"""Thin ctypes binding of the C ABI in include/tgemm.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  There is no CPU fallback; if the library cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+TGEMM_F16, TGEMM_BF16 = 0, 1
+TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_RELU = 0, 1, 2, 3
+STATUS = {0: "TGEMM_OK", 1: "TGEMM_ERR_INVALID_ARG", 2: "TGEMM_ERR_ALIGNMENT",
+          3: "TGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TGEMM_ERR_ALIAS", 5: "TGEMM_ERR_CUDA",
+          6: "TGEMM_ERR_TIMEOUT"}
+EXPORTED = ("tgemm_run", "tgemm_run_host", "tgemm_status_string", "tgemm_last_device_status",
+            "tgemm_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TgemmError(RuntimeError):
+    def __init__(self, status: int, where: str = "tgemm_run"):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(self.status, self.status)}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libtgemm.so (building it with nvcc if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing:
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"CUDA library {_build.LIB} is missing; run build() first")
+        lib = ctypes.CDLL(_build.LIB)
+        p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        for name in ("tgemm_run", "tgemm_run_host"):
+            f = getattr(lib, name)
+            f.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p]
+            f.restype = i32
+        lib.tgemm_status_string.argtypes = [i32]
+        lib.tgemm_status_string.restype = ctypes.c_char_p
+        lib.tgemm_last_device_status.argtypes = []
+        lib.tgemm_last_device_status.restype = i32
+        lib.tgemm_version.argtypes = []
+        lib.tgemm_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def tgemm_run(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+              ldc: int, dtype: int, epilogue: int, stream: int = 0) -> int:
+    """Raw C-ABI call with device pointers (ints); returns the status code."""
+    return load().tgemm_run(A or None, B or None, bias or None, C or None, M, N, K, lda, ldb, ldc,
+                            dtype, epilogue, stream or None)
+
+
+def tgemm_run_host(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                   ldc: int, dtype: int, epilogue: int, stream: int = 0) -> int:
+    """Raw C-ABI call with host pointers (ints); returns the status code."""
+    return load().tgemm_run_host(A or None, B or None, bias or None, C or None, M, N, K, lda, ldb,
+                                 ldc, dtype, epilogue, stream or None)
+
+
+def tgemm_status_string(status: int) -> str:
+    return load().tgemm_status_string(int(status)).decode()
+
+
+def tgemm_last_device_status() -> int:
+    return int(load().tgemm_last_device_status())
+
+
+def tgemm_version() -> int:
+    return int(load().tgemm_version())

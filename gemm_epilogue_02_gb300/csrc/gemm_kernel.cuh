@@ -1,0 +1,391 @@
+// Persistent, warp-specialised tcgen05 GEMM with the epilogue fused in-kernel:
+//
+//     C[i, j] = epi( sum_k A[i, k] * B[k, j] (+ bias[j]) ),  epi in {identity, ReLU}
+//
+// This is the tile loop of the C = ReLU(A @ B) kernel of "Writing
+// high-performance kernels in TileLang" ("Écrivons un GEMM": clear the
+// accumulator, pipelined global -> shared copies of the A and B tiles, tile
+// MMA, activation, store) and of the bias epilogue of "从零开始学习 TileLang…"
+// §10.8 / "TileLang で GPU カーネル設計を解説" §4 (bias indexed by the output
+// column, added to the fp32 accumulator before the activation, one rounding at
+// the store), laid out for sm_103a instead of the pages' register-fragment
+// design:
+//
+//   warp 0      TMA producer: A tile [128 x 64] (K-major) and B tile [64 x BN]
+//               (N-major, as BN/64 sub-tiles of 64 columns) per k-block into a
+//               STAGES-deep shared-memory ring, 128-byte swizzled; full/empty
+//               mbarriers per stage (the software pipeline of T.Pipelined).
+//   warp 1      allocates TMEM (two BN-column fp32 accumulators) and one lane
+//               issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide k step; a
+//               tcgen05.commit frees each ring stage and publishes each
+//               finished accumulator.
+//   warps 2..5  epilogue: tcgen05.ld TMEM -> registers (each warp owns the 32
+//               TMEM lanes = 32 rows its warp index allows), + bias, ReLU,
+//               round to fp16/bf16, 128B-swizzled staging in shared memory,
+//               then a TMA store (clipped at ragged M/N edges) or, when C's
+//               pitch is not 16-byte aligned, masked coalesced stores.
+//
+// Tiles are visited in a grouped order (GROUP_M row-blocks per column sweep,
+// the L2 block swizzle of T.use_swizzle) by a persistent grid of at most one
+// CTA per SM; the epilogue of tile i overlaps the MMAs of tile i+1 through the
+// two TMEM accumulators.
+//
+// Every mbarrier wait is bounded by a wall-clock limit: on expiry the waiter
+// records TGEMM_ERR_TIMEOUT in the device status word, raises a CTA-wide abort
+// flag, and all roles drain their in-flight copies / MMAs and return, so a
+// broken pipeline ends the kernel instead of hanging the GPU.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace tgemm {
+
+constexpr int kBM = 128;          // rows per tile (TMEM lanes)
+constexpr int kBK = 64;           // k per ring stage: 64 x 2 B = one 128-byte swizzle row
+constexpr int kUmmaK = 16;        // k per tcgen05.mma (kind::f16)
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kEpiWarps = 4;
+constexpr uint32_t kCStageBytes = 32 * 128;   // 32 rows x 64 columns x 2 B
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr uint32_t kStatusTimeout = 6;             // TGEMM_ERR_TIMEOUT
+
+struct KParams {
+    int M, N, K;
+    int num_m, num_n, num_kb, num_tiles, group_m;
+    const void *bias;          // may be null when !has_bias
+    void *C;                   // used by the masked-store path only
+    long long ldc;
+    int has_bias, relu, is_bf16, tma_store;
+    uint32_t idesc;
+    unsigned int *status;      // device status word
+};
+
+template <int BN, int STAGES>
+struct Smem {
+    static constexpr uint32_t kABytes = kBM * kBK * 2;          // 16 KiB
+    static constexpr uint32_t kBBytes = kBK * BN * 2;           // BN/64 sub-tiles of 8 KiB
+    static constexpr uint32_t kStageTx = kABytes + kBBytes;
+    static constexpr uint32_t kOffA = 0;
+    static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
+    static constexpr uint32_t kOffC = kOffB + STAGES * kBBytes;
+    static constexpr uint32_t kOffBar = kOffC + kEpiWarps * 2 * kCStageBytes;
+    // full[S], empty[S], tfull[2], tempty[2], drain
+    static constexpr uint32_t kNumBars = 2 * STAGES + 5;
+    static constexpr uint32_t kOffTmemHolder = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
+    static constexpr uint32_t kBytes = kOffAbort + 4;
+    static constexpr uint32_t kDynamicBytes = kBytes + 1024;   // 1 KiB alignment slack
+    static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
+                                          : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    static_assert(kDynamicBytes <= 232448, "shared memory budget exceeded");
+    static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "swizzled buffers need 1 KiB alignment");
+};
+
+// Bounded wait.  Returns false if the CTA is aborting or the limit ran out.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         unsigned int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 127u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicExch(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait used only while draining after an abort (ignores the flag).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+__device__ __forceinline__ void tile_coords(int t, const KParams &p, int &m_blk, int &n_blk) {
+    const int per_group = p.group_m * p.num_n;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int gsize = min(p.num_m - first_m, p.group_m);
+    const int local = t - g * per_group;
+    m_blk = first_m + local % gsize;
+    n_blk = local / gsize;
+}
+
+__device__ __forceinline__ float bias_val(const void *bias, int idx, int is_bf16) {
+    const unsigned short raw = __ldg(reinterpret_cast<const unsigned short *>(bias) + idx);
+    return is_bf16 ? __bfloat162float(__ushort_as_bfloat16(raw)) : __half2float(__ushort_as_half(raw));
+}
+
+__device__ __forceinline__ float epi_relu(float v) {
+    // x <= 0 (incl. -0.0) -> +0.0; NaN compares false and is kept.
+    return (v <= 0.0f) ? 0.0f : v;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
+    if (is_bf16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    tgemm_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC, const KParams p) {
+    using L = Smem<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::kOffBar;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kOffTmemHolder);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffAbort);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_shared();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        if (p.tma_store) prefetch_tmap(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t uses[STAGES];
+            for (int s = 0; s < STAGES; ++s) uses[s] = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                int m_blk, n_blk;
+                tile_coords(t, p, m_blk, n_blk);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, L::kStageTx);
+                    const uint32_t a_dst = sbase + L::kOffA + stage * L::kABytes;
+                    const uint32_t b_dst = sbase + L::kOffB + stage * L::kBBytes;
+                    tma_load_2d(a_dst, &tmA, fb, kb * kBK, m_blk * kBM);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(b_dst + j * (kBK * 128), &tmB, fb, n_blk * BN + j * 64, kb * kBK);
+                    ++uses[stage];
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // Let every copy this thread started land before the CTA exits.
+                for (int s = 0; s < STAGES; ++s)
+                    if (uses[s]) drain_wait(full_bar(s), (uses[s] - 1u) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = sbase + L::kOffA + stage * L::kABytes;
+                    const uint32_t b_addr = sbase + L::kOffB + stage * L::kBBytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        // A: K-major, 8-row groups 1 KiB apart; a 16-wide k step is 32 B along the row.
+                        const uint64_t adesc = sw128_desc(a_addr + k * (kUmmaK * 2), 16, 1024);
+                        // B: N-major; 64-column sub-tiles kBK*128 B apart (leading), 8-row k groups
+                        // 1 KiB apart (stride); a 16-wide k step is 16 rows = 2 KiB.
+                        const uint64_t bdesc = sw128_desc(b_addr + k * (kUmmaK * 128), kBK * 128, 1024);
+                        mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(stage));          // frees the ring stage once read
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(acc));                // accumulator ready for the epilogue
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            // All MMAs issued by this thread complete before TMEM is released.
+            mma_commit(drain_bar);
+            drain_wait(drain_bar, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                  // TMEM lane quarter this warp may access
+        const int ew = warp - 2;                 // epilogue warp index 0..3
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int buf = 0;
+        const uint32_t cstage0 = sbase + L::kOffC + ew * 2 * kCStageBytes;
+        uint8_t *cstage_gen0 = smem + L::kOffC + ew * 2 * kCStageBytes;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            int m_blk, n_blk;
+            tile_coords(t, p, m_blk, n_blk);
+            int ok = 1;
+            if (lane == 0) ok = wait_bar(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int m0 = m_blk * kBM + q * 32;
+            const int n_tile = n_blk * BN;
+            // Only chunks / rows that intersect C are read out and stored (no
+            // store is ever issued at a coordinate outside the tensor).
+            const int c_end = (m0 < p.M) ? min(BN / 64, (p.N - n_tile + 63) / 64) : 0;
+            if (c_end == 0) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+            }
+#pragma unroll 1
+            for (int c = 0; c < c_end; ++c) {
+                uint32_t r[64];
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(acc * BN + c * 64);
+                tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                tmem_wait_ld();
+                if (c == c_end - 1) {
+                    // Last read of this accumulator: hand it back to the MMA warp.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(acc));
+                }
+                const int n0 = n_tile + c * 64;
+                uint32_t packed[32];
+                const bool full_bias = p.has_bias && (n0 + 64 <= p.N);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    float bv[8];
+                    if (full_bias) {
+                        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+                                                    reinterpret_cast<const unsigned short *>(p.bias) + n0) +
+                                                g);
+                        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const unsigned short lo = static_cast<unsigned short>(w[h] & 0xFFFFu);
+                            const unsigned short hi = static_cast<unsigned short>(w[h] >> 16);
+                            if (p.is_bf16) {
+                                bv[2 * h] = __bfloat162float(__ushort_as_bfloat16(lo));
+                                bv[2 * h + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
+                            } else {
+                                bv[2 * h] = __half2float(__ushort_as_half(lo));
+                                bv[2 * h + 1] = __half2float(__ushort_as_half(hi));
+                            }
+                        }
+                    } else if (p.has_bias) {
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) {
+                            const int col = n0 + g * 8 + h;
+                            bv[h] = (col < p.N) ? bias_val(p.bias, col, p.is_bf16) : 0.0f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) bv[h] = 0.0f;
+                    }
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        float v0 = __uint_as_float(r[g * 8 + 2 * h]) + bv[2 * h];
+                        float v1 = __uint_as_float(r[g * 8 + 2 * h + 1]) + bv[2 * h + 1];
+                        if (p.relu) { v0 = epi_relu(v0); v1 = epi_relu(v1); }
+                        packed[g * 4 + h] = pack2(v0, v1, p.is_bf16);
+                    }
+                }
+                // Stage the 32 x 64 block: row `lane`, 16-byte chunk j at (j ^ (lane & 7)).
+                const uint32_t sb = cstage0 + buf * kCStageBytes;
+                uint8_t *sb_gen = cstage_gen0 + buf * kCStageBytes;
+                if (p.tma_store && lane == 0) bulk_wait_group_read<1>();   // buffer reused 2 stores later
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t addr = sb + lane * 128 + ((j ^ (lane & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                 "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
+                                 "r"(packed[4 * j + 3])
+                                 : "memory");
+                }
+                if (p.tma_store) {
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, sb, n0, m0);
+                        bulk_commit_group();
+                    }
+                } else {
+                    __syncwarp();
+                    // Masked, coalesced 2-byte stores: lane l writes columns 2l, 2l+1 of each row.
+                    unsigned short *Cg = reinterpret_cast<unsigned short *>(p.C);
+                    const int col = n0 + 2 * lane;
+#pragma unroll 4
+                    for (int rr = 0; rr < 32; ++rr) {
+                        const int row = m0 + rr;
+                        if (row >= p.M) break;
+                        const uint32_t v = *reinterpret_cast<const uint32_t *>(
+                            sb_gen + rr * 128 + ((((lane >> 2) ^ (rr & 7)) << 4) | ((lane & 3) << 2)));
+                        unsigned short *dst = Cg + static_cast<long long>(row) * p.ldc + col;
+                        if (col < p.N) dst[0] = static_cast<unsigned short>(v & 0xFFFFu);
+                        if (col + 1 < p.N) dst[1] = static_cast<unsigned short>(v >> 16);
+                    }
+                }
+                buf ^= 1;
+            }
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (p.tma_store && lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, L::kTmemCols);
+}
+
+}  // namespace tgemm

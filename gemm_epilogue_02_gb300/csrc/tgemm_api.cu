@@ -1,0 +1,429 @@
+// C-ABI of the fused GEMM epilogue library (declarations and contract in
+// include/tgemm.h): argument validation, device checks, tensor-map encoding,
+// tile-configuration choice, operand repacking for unaligned pitches and the
+// launches.  No CPU fallback exists: every result is computed by the kernels
+// in this library.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/tgemm.h"
+#include "aux_kernels.cuh"
+#include "gemm_kernel.cuh"
+
+namespace tgemm {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kVersion = 0x000100;
+
+__device__ unsigned int g_device_status;
+
+struct DeviceInfo {
+    std::once_flag once;
+    bool ok = false;        // CC 10.3
+    int num_sms = 0;
+    unsigned int *status = nullptr;
+    cudaMemPool_t pool = nullptr;
+    std::mutex mu;          // guards lazily set kernel attributes
+    unsigned attr_set = 0;  // bit per kernel configuration
+};
+
+DeviceInfo g_dev[kMaxDevices];
+
+bool device_info(int dev, DeviceInfo **out) {
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    DeviceInfo &d = g_dev[dev];
+    std::call_once(d.once, [&]() {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        if (major != 10 || minor != 3) return;
+        void *sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        uint64_t keep = UINT64_MAX;   // keep freed scratch in the pool for the next call
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        d.num_sms = sms;
+        d.status = static_cast<unsigned int *>(sym);
+        d.pool = pool;
+        d.ok = true;
+    });
+    *out = &d;
+    return d.ok;
+}
+
+tgemm_status current_device(DeviceInfo **d) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (!device_info(dev, d)) return TGEMM_ERR_UNSUPPORTED_DEVICE;
+    return TGEMM_OK;
+}
+
+// ---------------------------------------------------------------- validation
+struct Range {
+    uintptr_t lo, hi;
+};
+
+Range span(const void *p, int64_t rows, int64_t ld, int64_t width) {
+    const uintptr_t b = reinterpret_cast<uintptr_t>(p);
+    if (rows <= 0 || width <= 0) return {b, b};
+    return {b, b + static_cast<uintptr_t>(((rows - 1) * ld + width) * 2)};
+}
+
+bool overlaps(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tgemm_status validate(const void *A, const void *B, const void *bias, const void *C, int64_t M,
+                      int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int dtype,
+                      int epilogue) {
+    if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return TGEMM_ERR_INVALID_ARG;
+    if (lda < K || ldb < N || ldc < N) return TGEMM_ERR_INVALID_ARG;
+    if (lda > (int64_t(1) << 40) || ldb > (int64_t(1) << 40) || ldc > (int64_t(1) << 40))
+        return TGEMM_ERR_INVALID_ARG;
+    if (dtype != TGEMM_F16 && dtype != TGEMM_BF16) return TGEMM_ERR_INVALID_ARG;
+    if (epilogue < TGEMM_EPI_NONE || epilogue > TGEMM_EPI_BIAS_RELU) return TGEMM_ERR_INVALID_ARG;
+    const bool use_bias = epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU;
+    if (M == 0 || N == 0) return TGEMM_OK;
+    if (C == nullptr) return TGEMM_ERR_INVALID_ARG;
+    if (K > 0 && (A == nullptr || B == nullptr)) return TGEMM_ERR_INVALID_ARG;
+    if (use_bias && bias == nullptr) return TGEMM_ERR_INVALID_ARG;
+    if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))) ||
+        (use_bias && !aligned16(bias)))
+        return TGEMM_ERR_ALIGNMENT;
+    const Range rc = span(C, M, ldc, N);
+    if (K > 0 && (overlaps(rc, span(A, M, lda, K)) || overlaps(rc, span(B, K, ldb, N))))
+        return TGEMM_ERR_ALIAS;
+    if (use_bias && overlaps(rc, span(bias, 1, N, N))) return TGEMM_ERR_ALIAS;
+    return TGEMM_OK;
+}
+
+bool is_device_memory(const void *p, int dev) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (at.type == cudaMemoryTypeManaged) return true;
+    return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, []() {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Row-major [rows x cols] 16-bit matrix with pitch `ld`, box [box_rows x box_cols].
+bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld,
+              uint32_t box_cols, uint32_t box_rows, bool bf16) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- configs
+struct Cfg {
+    int bn;
+    int stages;
+    int bit;
+};
+constexpr Cfg kCfg256 = {256, 4, 1};
+constexpr Cfg kCfg128 = {128, 6, 2};
+constexpr Cfg kCfg64 = {64, 8, 4};
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+Cfg choose_config(int64_t M, int64_t N, int num_sms) {
+    if (const char *f = std::getenv("TGEMM_FORCE_BN")) {
+        const int bn = std::atoi(f);
+        if (bn == 256) return kCfg256;
+        if (bn == 128) return kCfg128;
+        if (bn == 64) return kCfg64;
+    }
+    const int64_t mt = cdiv(M, kBM);
+    if (mt * cdiv(N, 256) >= num_sms) return kCfg256;
+    if (mt * cdiv(N, 128) >= num_sms) return kCfg128;
+    return kCfg64;
+}
+
+template <int BN, int ST>
+cudaError_t launch_fused(DeviceInfo *d, int bit, const CUtensorMap &ta, const CUtensorMap &tb,
+                         const CUtensorMap &tc, const KParams &p, int grid, cudaStream_t s) {
+    using L = Smem<BN, ST>;
+    {
+        std::lock_guard<std::mutex> g(d->mu);
+        if (!(d->attr_set & bit)) {
+            cudaError_t e = cudaFuncSetAttribute(tgemm_fused_kernel<BN, ST>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 L::kDynamicBytes);
+            if (e != cudaSuccess) return e;
+            d->attr_set |= bit;
+        }
+    }
+    tgemm_fused_kernel<BN, ST><<<grid, kThreads, L::kDynamicBytes, s>>>(ta, tb, tc, p);
+    return cudaGetLastError();
+}
+
+cudaError_t repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows, int64_t cols,
+                   cudaStream_t s) {
+    const dim3 block(256);
+    const dim3 grid(static_cast<unsigned>(std::min<int64_t>(cdiv(cols, 256), 64)),
+                    static_cast<unsigned>(std::min<int64_t>(rows, 65535)));
+    repack_rows_kernel<<<grid, block, 0, s>>>(static_cast<const uint16_t *>(src), lds,
+                                              static_cast<uint16_t *>(dst), ldd, rows, cols);
+    return cudaGetLastError();
+}
+
+tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void *bias, void *C,
+                        int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        int dtype, int epilogue, cudaStream_t stream) {
+    const bool bf16 = dtype == TGEMM_BF16;
+    const int has_bias = (epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU) ? 1 : 0;
+    const int relu = (epilogue == TGEMM_EPI_RELU || epilogue == TGEMM_EPI_BIAS_RELU) ? 1 : 0;
+    if (M == 0 || N == 0) return TGEMM_OK;
+    if (K == 0) {
+        const dim3 grid(static_cast<unsigned>(std::min<int64_t>(cdiv(N, 256), 64)),
+                        static_cast<unsigned>(std::min<int64_t>(M, 65535)));
+        fill_epilogue_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t *>(bias),
+                                                       static_cast<uint16_t *>(C), ldc,
+                                                       static_cast<int>(M), static_cast<int>(N),
+                                                       has_bias, relu, bf16 ? 1 : 0);
+        return cudaGetLastError() == cudaSuccess ? TGEMM_OK : TGEMM_ERR_CUDA;
+    }
+
+    // Operands whose pitch is not a multiple of 16 bytes are repacked first.
+    void *scratch_a = nullptr, *scratch_b = nullptr;
+    const void *a_use = A, *b_use = B;
+    int64_t lda_use = lda, ldb_use = ldb;
+    tgemm_status st = TGEMM_OK;
+    auto release = [&]() {
+        if (scratch_a) cudaFreeAsync(scratch_a, stream);
+        if (scratch_b) cudaFreeAsync(scratch_b, stream);
+    };
+    if (lda % 8 != 0) {
+        lda_use = cdiv(K, 8) * 8;
+        if (cudaMallocFromPoolAsync(&scratch_a, static_cast<size_t>(M * lda_use * 2), d->pool,
+                                    stream) != cudaSuccess ||
+            repack(A, lda, scratch_a, lda_use, M, K, stream) != cudaSuccess)
+            st = TGEMM_ERR_CUDA;
+        a_use = scratch_a;
+    }
+    if (st == TGEMM_OK && ldb % 8 != 0) {
+        ldb_use = cdiv(N, 8) * 8;
+        if (cudaMallocFromPoolAsync(&scratch_b, static_cast<size_t>(K * ldb_use * 2), d->pool,
+                                    stream) != cudaSuccess ||
+            repack(B, ldb, scratch_b, ldb_use, K, N, stream) != cudaSuccess)
+            st = TGEMM_ERR_CUDA;
+        b_use = scratch_b;
+    }
+    if (st != TGEMM_OK) {
+        cudaGetLastError();
+        release();
+        return st;
+    }
+
+    const Cfg cfg = choose_config(M, N, d->num_sms);
+    const bool tma_store = (ldc % 8) == 0;
+    CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    if (!make_map(&ta, a_use, M, K, lda_use, kBK, kBM, bf16) ||
+        !make_map(&tb, b_use, K, N, ldb_use, 64, kBK, bf16) ||
+        (tma_store && !make_map(&tc, C, M, N, ldc, 64, 32, bf16))) {
+        release();
+        return TGEMM_ERR_CUDA;
+    }
+
+    KParams p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_m = static_cast<int>(cdiv(M, kBM));
+    p.num_n = static_cast<int>(cdiv(N, cfg.bn));
+    p.num_kb = static_cast<int>(cdiv(K, kBK));
+    const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+    if (tiles > INT32_MAX) {
+        release();
+        return TGEMM_ERR_INVALID_ARG;
+    }
+    p.num_tiles = static_cast<int>(tiles);
+    p.group_m = std::min(p.num_m, 16);
+    p.bias = bias;
+    p.C = C;
+    p.ldc = ldc;
+    p.has_bias = has_bias;
+    p.relu = relu;
+    p.is_bf16 = bf16 ? 1 : 0;
+    p.tma_store = tma_store ? 1 : 0;
+    p.idesc = idesc_f16(bf16, kBM, static_cast<uint32_t>(cfg.bn), false, true);
+    p.status = d->status;
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, d->num_sms));
+
+    cudaError_t e;
+    switch (cfg.bn) {
+        case 256: e = launch_fused<256, 4>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
+        case 128: e = launch_fused<128, 6>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
+        default: e = launch_fused<64, 8>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
+    }
+    release();
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
+}
+
+}  // namespace
+}  // namespace tgemm
+
+using namespace tgemm;
+
+extern "C" tgemm_status tgemm_run(const void *A, const void *B, const void *bias, void *C,
+                                  int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                  int64_t ldc, tgemm_dtype dtype, tgemm_epilogue epilogue,
+                                  tgemm_stream_t stream) {
+    tgemm_status st = validate(A, B, bias, C, M, N, K, lda, ldb, ldc, dtype, epilogue);
+    if (st != TGEMM_OK) return st;
+    DeviceInfo *d = nullptr;
+    st = current_device(&d);
+    if (st != TGEMM_OK) return st;
+    if (M == 0 || N == 0) return TGEMM_OK;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool use_bias = epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU;
+    if (!is_device_memory(C, dev) || (K > 0 && (!is_device_memory(A, dev) || !is_device_memory(B, dev))) ||
+        (use_bias && !is_device_memory(bias, dev)))
+        return TGEMM_ERR_INVALID_ARG;
+    return run_device(d, A, B, bias, C, M, N, K, lda, ldb, ldc, dtype, epilogue,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" tgemm_status tgemm_run_host(const void *A_host, const void *B_host,
+                                       const void *bias_host, void *C_host, int64_t M, int64_t N,
+                                       int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                       tgemm_dtype dtype, tgemm_epilogue epilogue,
+                                       tgemm_stream_t stream_) {
+    tgemm_status st = validate(A_host, B_host, bias_host, C_host, M, N, K, lda, ldb, ldc, dtype,
+                               epilogue);
+    if (st != TGEMM_OK) return st;
+    DeviceInfo *d = nullptr;
+    st = current_device(&d);
+    if (st != TGEMM_OK) return st;
+    if (M == 0 || N == 0) return TGEMM_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const bool use_bias = epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU;
+    void *dA = nullptr, *dB = nullptr, *dbias = nullptr, *dC = nullptr;
+    bool ok = true;
+    auto alloc = [&](void **p, size_t bytes) {
+        if (ok && cudaMallocFromPoolAsync(p, bytes, d->pool, stream) != cudaSuccess) ok = false;
+    };
+    if (K > 0) {
+        alloc(&dA, static_cast<size_t>(M * lda * 2));
+        alloc(&dB, static_cast<size_t>(K * ldb * 2));
+    }
+    if (use_bias) alloc(&dbias, static_cast<size_t>(N * 2));
+    alloc(&dC, static_cast<size_t>(M * ldc * 2));
+    if (ok && K > 0) {
+        ok = cudaMemcpy2DAsync(dA, lda * 2, A_host, lda * 2, K * 2, M, cudaMemcpyHostToDevice,
+                               stream) == cudaSuccess &&
+             cudaMemcpy2DAsync(dB, ldb * 2, B_host, ldb * 2, N * 2, K, cudaMemcpyHostToDevice,
+                               stream) == cudaSuccess;
+    }
+    if (ok && use_bias)
+        ok = cudaMemcpyAsync(dbias, bias_host, N * 2, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+    if (ok) {
+        st = run_device(d, dA, dB, dbias, dC, M, N, K, lda, ldb, ldc, dtype, epilogue, stream);
+        if (st == TGEMM_OK &&
+            cudaMemcpy2DAsync(C_host, ldc * 2, dC, ldc * 2, N * 2, M, cudaMemcpyDeviceToHost,
+                              stream) != cudaSuccess)
+            st = TGEMM_ERR_CUDA;
+    } else {
+        st = TGEMM_ERR_CUDA;
+    }
+    for (void *p : {dA, dB, dbias, dC})
+        if (p) cudaFreeAsync(p, stream);
+    if (st != TGEMM_OK) cudaGetLastError();
+    return st;
+}
+
+extern "C" const char *tgemm_status_string(tgemm_status s) {
+    switch (s) {
+        case TGEMM_OK: return "TGEMM_OK";
+        case TGEMM_ERR_INVALID_ARG: return "TGEMM_ERR_INVALID_ARG: bad size, pitch, pointer, dtype or epilogue";
+        case TGEMM_ERR_ALIGNMENT: return "TGEMM_ERR_ALIGNMENT: a base pointer is not 16-byte aligned";
+        case TGEMM_ERR_UNSUPPORTED_DEVICE: return "TGEMM_ERR_UNSUPPORTED_DEVICE: needs a CC 10.3 (sm_103a) GPU";
+        case TGEMM_ERR_ALIAS: return "TGEMM_ERR_ALIAS: C overlaps an input";
+        case TGEMM_ERR_CUDA: return "TGEMM_ERR_CUDA: a CUDA call or launch failed";
+        case TGEMM_ERR_TIMEOUT: return "TGEMM_ERR_TIMEOUT: a kernel gave up on a pipeline wait";
+    }
+    return "TGEMM_ERR_UNKNOWN";
+}
+
+extern "C" tgemm_status tgemm_last_device_status(void) {
+    DeviceInfo *d = nullptr;
+    tgemm_status st = current_device(&d);
+    if (st != TGEMM_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpy(&v, d->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return v ? static_cast<tgemm_status>(v) : TGEMM_OK;
+}
+
+extern "C" int tgemm_version(void) { return kVersion; }

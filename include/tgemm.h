@@ -1,0 +1,125 @@
+/*
+ * tgemm — fused tensor-core GEMM with an in-kernel epilogue, for GB300 (sm_103a).
+ *
+ *     C[i, j] = epi( sum_{k<K} A[i, k] * B[k, j]  (+ bias[j]) )    0 <= i < M, 0 <= j < N
+ *
+ * The operation is the GEMM of "从零开始学习 TileLang：从 Python、PyTorch 到高性能
+ * GPU Kernel 的完整开发教程", ch.10 §10.1 (C_ij = sum_k A_ik B_kj, 2MNK flops,
+ * §10.9), with the epilogue of its §10.8 "GEMM Epilogue 融合" (relu(a @ b + bias),
+ * bias indexed by the output column, applied before the write-back), the
+ * C = ReLU(A @ B) kernel of "Writing high-performance kernels in TileLang"
+ * ("Écrivons un GEMM"), the Bias (N,) operand of "TileLang で GPU カーネル設計を
+ * 解説" §4, and the load -> GEMM -> activation -> store tile fusion of
+ * "【CUDA】TileFusion".  Precision follows the tutorial's §10.7 recipe: fp16 or
+ * bf16 inputs, tensor-core products, fp32 accumulation, one final rounding to
+ * the input dtype (round to nearest even).  ReLU maps x <= 0 (including -0.0)
+ * to +0.0 and keeps NaN.
+ *
+ * Layout: every matrix is row-major with an explicit leading dimension (row
+ * pitch, in elements): A[i, k] at A + i*lda + k, B[k, j] at B + k*ldb + j,
+ * C[i, j] at C + i*ldc + j.  bias has N contiguous elements.  All four arrays
+ * hold the same dtype.  Elements of C outside 0 <= j < N (the pitch padding)
+ * are never written.
+ *
+ * Ownership: the caller owns every buffer; the library never frees, retains or
+ * reads a pointer after the enqueued work completes.
+ */
+#ifndef TGEMM_H
+#define TGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *tgemm_stream_t;   /* same handle as cudaStream_t; NULL = legacy default stream */
+
+typedef enum { TGEMM_F16 = 0, TGEMM_BF16 = 1 } tgemm_dtype;
+
+typedef enum {
+    TGEMM_EPI_NONE = 0,       /* C = A.B                 */
+    TGEMM_EPI_RELU = 1,       /* C = max(A.B, 0)         */
+    TGEMM_EPI_BIAS = 2,       /* C = A.B + bias          */
+    TGEMM_EPI_BIAS_RELU = 3   /* C = max(A.B + bias, 0)  */
+} tgemm_epilogue;
+
+typedef enum {
+    TGEMM_OK = 0,
+    TGEMM_ERR_INVALID_ARG = 1,        /* bad size, pitch, NULL pointer, dtype or epilogue   */
+    TGEMM_ERR_ALIGNMENT = 2,          /* a base pointer is not 16-byte aligned               */
+    TGEMM_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or the current device is not CC 10.3 */
+    TGEMM_ERR_ALIAS = 4,              /* C's byte range overlaps A, B or bias                */
+    TGEMM_ERR_CUDA = 5,               /* a CUDA runtime/driver call or a launch failed       */
+    TGEMM_ERR_TIMEOUT = 6             /* a kernel gave up on a pipeline wait (device status) */
+} tgemm_status;
+
+/*
+ * tgemm_run — enqueue C = epi(A.B + bias) on `stream` (device pointers).
+ *
+ * Arguments: A [M x lda], B [K x ldb], bias [N] (may be NULL unless the
+ * epilogue uses it), C [M x ldc], all device pointers in `dtype`.
+ *
+ * Errors are reported synchronously, before anything is enqueued, and leave C
+ * untouched:
+ *   M, N or K < 0; lda < K, ldb < N or ldc < N; a NULL A, B or C when the
+ *   problem is not empty; a NULL bias with a BIAS epilogue; an unknown dtype or
+ *   epilogue                                              -> TGEMM_ERR_INVALID_ARG
+ *   a base pointer (A, B, C, bias) not 16-byte aligned    -> TGEMM_ERR_ALIGNMENT
+ *   C's byte range overlapping A's, B's or bias's         -> TGEMM_ERR_ALIAS
+ *   no device, or a current device other than CC 10.3    -> TGEMM_ERR_UNSUPPORTED_DEVICE
+ *   a pointer the driver does not know as device memory   -> TGEMM_ERR_INVALID_ARG
+ *   a failed CUDA call or launch                          -> TGEMM_ERR_CUDA
+ *
+ * Degenerate sizes: M == 0 or N == 0 enqueues nothing and returns TGEMM_OK;
+ * K == 0 writes epi(bias) (the empty sum is 0).
+ *
+ * Any pitch >= the logical width is accepted.  When lda or ldb is not a
+ * multiple of 8 elements (tensor-memory-access copies need 16-byte row
+ * strides) the operand is first repacked on the GPU into a 16-byte-pitched
+ * scratch buffer drawn stream-ordered from a library-owned memory pool and
+ * returned to it on `stream`; when ldc is not a multiple of 8 the epilogue
+ * stores C with plain masked stores instead of tensor-memory-access stores.
+ *
+ * Asynchrony: returns once the work is enqueued; the caller synchronises.
+ * Thread safety: safe to call from several host threads.
+ */
+tgemm_status tgemm_run(const void *A, const void *B, const void *bias, void *C,
+                       int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc,
+                       tgemm_dtype dtype, tgemm_epilogue epilogue, tgemm_stream_t stream);
+
+/*
+ * tgemm_run_host — the same operation on HOST buffers (pinned or pageable),
+ * end to end: device buffers are drawn from the library's stream-ordered pool,
+ * A, B and bias are copied host -> device on `stream`, tgemm_run is enqueued,
+ * C is copied device -> host, and the buffers are returned to the pool.
+ * The call returns after enqueueing; C_host is valid once `stream` has been
+ * synchronised (with pageable memory the copies themselves may block).
+ * Same arguments, pitches and errors as tgemm_run (no device-pointer check).
+ */
+tgemm_status tgemm_run_host(const void *A_host, const void *B_host, const void *bias_host,
+                            void *C_host, int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldc,
+                            tgemm_dtype dtype, tgemm_epilogue epilogue, tgemm_stream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *tgemm_status_string(tgemm_status status);
+
+/*
+ * tgemm_last_device_status — read and clear the device-side status word of the
+ * current device.  Kernels bound every pipeline wait by a time limit; a wait
+ * that runs out records TGEMM_ERR_TIMEOUT here and the kernel returns early
+ * (its output is then invalid).  Synchronises the device.  Returns TGEMM_OK
+ * when no kernel has timed out since the last call.
+ */
+tgemm_status tgemm_last_device_status(void);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int tgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGEMM_H */

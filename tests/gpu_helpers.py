@@ -1,0 +1,98 @@
+"""Shared helpers of the GPU parity tests: seeded inputs -> device (with the
+requested pitches) -> C-ABI call -> comparison against the fp64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import seeded_inputs as si
+
+EPI = {"none": 0, "relu": 1, "bias": 2, "bias_relu": 3}
+ODT = {"fp16": oracle.F16, "bf16": oracle.BF16}
+TDT = {"fp16": torch.float16, "bf16": torch.bfloat16}
+SENTINEL = 0x7E5A          # a NaN bit pattern in both fp16 and bf16; must survive in C's pad
+
+# Bounds from the method's evaluation: relative Frobenius <= 2e-3 and
+# |err| <= 1e-2 + 1e-2 |ref| per element, against the unrounded fp64 oracle.
+FROB_TOL = 2e-3
+ATOL, RTOL = 1e-2, 1e-2
+
+
+def to_device_pitched(x: torch.Tensor, width: int) -> torch.Tensor:
+    """Copy a CPU [rows, ld] tensor to the GPU and return the [rows, width] view."""
+    d = x.to("cuda")
+    return d[:, :width]
+
+
+def alloc_c(M: int, N: int, ldc: int, dtype: str) -> torch.Tensor:
+    full = torch.full((max(M, 1), ldc), SENTINEL, dtype=torch.int16, device="cuda")
+    return full.view(TDT[dtype])[:M, :N]
+
+
+def c_bits(C: torch.Tensor, M: int, ldc: int) -> np.ndarray:
+    """All of C's rows including the pad columns, as uint16 [M, ldc]."""
+    base = C.as_strided((M, ldc), (ldc, 1)) if M > 0 else C
+    return base.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_tgemm(tg, M, N, K, dtype="fp16", epilogue="bias_relu", seed=0, kind="normal",
+              lda=None, ldb=None, ldc=None):
+    """Returns (A, B, bias) CPU inputs and the uint16 [M, ldc] result (pad included)."""
+    lda = lda or K
+    ldb = ldb or N
+    ldc = ldc or N
+    with_bias = epilogue in ("bias", "bias_relu")
+    A, B, bias = si.make_inputs(M, N, K, dtype, seed, kind, with_bias=True,
+                                lda=lda if lda != K else None, ldb=ldb if ldb != N else None)
+    Ad = to_device_pitched(A, K) if M * K > 0 else torch.empty((M, K), dtype=TDT[dtype], device="cuda")
+    Bd = to_device_pitched(B, N) if K * N > 0 else torch.empty((K, N), dtype=TDT[dtype], device="cuda")
+    biasd = bias.to("cuda") if with_bias else None
+    Cd = alloc_c(M, N, ldc, dtype)
+    tg.run(Ad, Bd, biasd, Cd, epilogue)
+    torch.cuda.synchronize()
+    return (A, B, bias if with_bias else None), c_bits(Cd, M, ldc)
+
+
+def oracle_ref(inputs, M, N, K, dtype, epilogue, rows=None):
+    A, B, bias = inputs
+    return oracle.gemm_epilogue_f64(si.bits(A) if M * K else None, si.bits(B) if K * N else None,
+                                    si.bits(bias) if bias is not None else None, M, N, K,
+                                    ODT[dtype], EPI[epilogue], rows=rows)
+
+
+def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(TDT[dtype])
+    return t.to(torch.float64).numpy()
+
+
+def assert_close(got_bits: np.ndarray, ref: np.ndarray, dtype: str, what=""):
+    got = decode(got_bits, dtype)
+    assert got.shape == ref.shape
+    finite = np.isfinite(ref)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), what
+    diff = np.abs(got[finite] - ref[finite])
+    rel = np.linalg.norm(diff) / max(np.linalg.norm(ref[finite]), 1e-12)
+    assert rel <= FROB_TOL, f"{what}: relative Frobenius error {rel:.3e}"
+    bad = diff > ATOL + RTOL * np.abs(ref[finite])
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements outside 1e-2 + 1e-2|ref|, max {diff.max():.3e}"
+    return rel
+
+
+def canon_zero(bits: np.ndarray) -> np.ndarray:
+    """-0.0 -> +0.0 (the sign of an exact zero sum is not fixed by the method)."""
+    b = bits.copy()
+    b[b == 0x8000] = 0
+    return b
+
+
+def assert_bit_exact(got_bits: np.ndarray, ref: np.ndarray, dtype: str, what=""):
+    want = oracle.round_to(ref, ODT[dtype])
+    g, w = canon_zero(got_bits), canon_zero(want)
+    mism = g != w
+    assert not mism.any(), f"{what}: {int(mism.sum())} mismatches, first at {np.argwhere(mism)[0]}"
+
+
+def assert_pad_untouched(bits_full: np.ndarray, N: int, what=""):
+    if bits_full.shape[1] > N:
+        assert (bits_full[:, N:] == SENTINEL).all(), f"{what}: C's pitch padding was written"

@@ -1,0 +1,184 @@
+"""GPU parity of the fused GEMM epilogue against the fp64 CPU oracle, through
+the C ABI.  Bit-exact on small-integer inputs; otherwise relative Frobenius
+<= 2e-3 and |err| <= 1e-2 + 1e-2 |ref| per element (against unrounded fp64).
+
+Coverage: the five workloads of the method's evaluation at their full sizes
+(sampled rows, every column), the integer-exact variant, a tiny / odd shape
+sweep (the tutorial's start-small advice and edge-case list), every epilogue x
+dtype, each tile configuration, wider pitches with guarded padding, K = 0 and
+empty problems, repeat-run determinism, the host-buffer entry point, and the
+device pointer check."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import seeded_inputs as si
+from gpu_helpers import (EPI, assert_bit_exact, assert_close, assert_pad_untouched, c_bits,
+                         oracle_ref, run_tgemm)
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_rows(M, n=48, seed=0):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, 129, M // 2, M - 129, M - 128, M - 2, M - 1]
+    rows = set(r for r in fixed if 0 <= r < M)
+    rows |= set(rng.choice(M, size=min(n, M), replace=False).tolist())
+    return sorted(rows)
+
+
+@pytest.fixture(autouse=True)
+def _lib(cuda_lib):
+    yield cuda_lib
+
+
+# ------------------------------------------------------------------ workloads
+@pytest.mark.parametrize("name", ["c0", "c1", "c2", "c3", "c4", "c4p"])
+def test_workload_full_size(cuda_lib, name):
+    w = si.WORKLOADS[name]
+    inputs, got = run_tgemm(cuda_lib, w.M, w.N, w.K, w.dtype, w.epilogue, w.seed, w.kind,
+                            w.lda, w.ldb, w.ldc)
+    ldc = w.ldc or w.N
+    assert_pad_untouched(got, w.N, name)
+    rows = list(range(w.M)) if w.M * w.N * w.K <= 2 ** 26 else sample_rows(w.M, seed=w.seed)
+    ref = oracle_ref(inputs, w.M, w.N, w.K, w.dtype, w.epilogue, rows=rows)
+    assert_close(got[rows, : w.N], ref, w.dtype, name)
+    del ldc
+
+
+def test_integer_exact_4096(cuda_lib):
+    w = si.WORKLOADS["c1x"]
+    for epi in ("bias_relu", "none"):
+        inputs, got = run_tgemm(cuda_lib, w.M, w.N, w.K, w.dtype, epi, w.seed, "int")
+        rows = sample_rows(w.M, n=40, seed=11)
+        ref = oracle_ref(inputs, w.M, w.N, w.K, w.dtype, epi, rows=rows)
+        assert_bit_exact(got[rows], ref, w.dtype, f"c1x {epi}")
+
+
+# ------------------------------------------------------------------ shapes
+SWEEP = [1, 2, 7, 8, 9, 63, 64, 65, 127, 128, 129, 255, 257]
+
+
+def sweep_cases(n=120):
+    rng = np.random.default_rng(2024)
+    cases = {(2, 8, 4), (1, 1, 1), (257, 257, 257), (1, 257, 257), (257, 1, 257), (257, 257, 1)}
+    while len(cases) < n:
+        cases.add(tuple(int(rng.choice(SWEEP)) for _ in range(3)))
+    return sorted(cases)
+
+
+@pytest.mark.parametrize("M,N,K", sweep_cases())
+def test_small_and_odd_shapes(cuda_lib, M, N, K):
+    idx = M * 7 + N * 3 + K
+    epi = ["none", "relu", "bias", "bias_relu"][idx % 4]
+    dtype = ["fp16", "bf16"][(idx // 4) % 2]
+    inputs, got = run_tgemm(cuda_lib, M, N, K, dtype, epi, seed=idx, kind="int")
+    ref = oracle_ref(inputs, M, N, K, dtype, epi)
+    assert_bit_exact(got, ref, dtype, f"{M}x{N}x{K} {epi} {dtype}")
+    inputs, got = run_tgemm(cuda_lib, M, N, K, dtype, epi, seed=idx)
+    ref = oracle_ref(inputs, M, N, K, dtype, epi)
+    assert_close(got, ref, dtype, f"{M}x{N}x{K} {epi} {dtype}")
+
+
+@pytest.mark.parametrize("bn", ["64", "128", "256"])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("epi", ["none", "relu", "bias", "bias_relu"])
+def test_each_tile_config_epilogue_dtype(cuda_lib, monkeypatch, bn, dtype, epi):
+    """Several tiles in both directions, a ragged tail on M, N and K, and a k
+    loop longer than the ring (so stages wrap) for each kernel configuration."""
+    monkeypatch.setenv("TGEMM_FORCE_BN", bn)
+    M, N, K = 333, 700, 1000
+    inputs, got = run_tgemm(cuda_lib, M, N, K, dtype, epi, seed=5, kind="int")
+    assert_bit_exact(got, oracle_ref(inputs, M, N, K, dtype, epi), dtype, f"int bn={bn}")
+    inputs, got = run_tgemm(cuda_lib, M, N, K, dtype, epi, seed=6)
+    assert_close(got, oracle_ref(inputs, M, N, K, dtype, epi), dtype, f"bn={bn}")
+
+
+@pytest.mark.parametrize("bn", ["64", "128", "256"])
+def test_persistent_loop_many_tiles(cuda_lib, monkeypatch, bn):
+    """More tiles than SMs: each CTA runs several tiles and both TMEM buffers."""
+    monkeypatch.setenv("TGEMM_FORCE_BN", bn)
+    M, N, K = 2560, 3072, 192
+    inputs, got = run_tgemm(cuda_lib, M, N, K, "bf16", "bias_relu", seed=9, kind="int")
+    assert_bit_exact(got, oracle_ref(inputs, M, N, K, "bf16", "bias_relu"), "bf16", f"bn={bn}")
+
+
+@pytest.mark.parametrize("lda,ldb,ldc", [(72, 136, 136), (75, 133, 131), (64, 129, 128),
+                                         (80, 128, 130)])
+def test_pitches_and_guarded_padding(cuda_lib, lda, ldb, ldc):
+    """Wider row pitches, aligned (TMA paths) and unaligned (repack / masked-store
+    paths); C's padding columns must keep their sentinel."""
+    M, N, K = 200, 128, 64
+    inputs, got = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=3, kind="int",
+                            lda=lda, ldb=ldb, ldc=ldc)
+    assert_pad_untouched(got, N, "pad")
+    assert_bit_exact(got[:, :N], oracle_ref(inputs, M, N, K, "fp16", "bias_relu"), "fp16", "pitch")
+
+
+# ------------------------------------------------------------------ degenerate
+@pytest.mark.parametrize("epi", ["none", "relu", "bias", "bias_relu"])
+def test_k_zero_writes_epilogue_of_bias(cuda_lib, epi):
+    M, N = 70, 90
+    inputs, got = run_tgemm(cuda_lib, M, N, 0, "bf16", epi, seed=4)
+    assert_bit_exact(got, oracle_ref(inputs, M, N, 0, "bf16", epi), "bf16", "K=0")
+
+
+def test_empty_problems_are_noops(cuda_lib):
+    for (M, N) in [(0, 64), (64, 0), (0, 0)]:
+        C = torch.full((max(M, 1), max(N, 1)), 7.0, dtype=torch.float16, device="cuda")
+        A = torch.ones((max(M, 1), 64), dtype=torch.float16, device="cuda")
+        B = torch.ones((64, max(N, 1)), dtype=torch.float16, device="cuda")
+        st = cuda_lib.tgemm_run(A.data_ptr(), B.data_ptr(), 0, C.data_ptr(), M, N, 64, 64,
+                                max(N, 1), max(N, 1), 0, 1, 0)
+        torch.cuda.synchronize()
+        assert st == 0 and (C == 7.0).all()
+
+
+# ------------------------------------------------------------------ invariants
+def test_relu_equals_max_of_none_bit_exact(cuda_lib):
+    M, N, K = 512, 768, 320
+    _, none = run_tgemm(cuda_lib, M, N, K, "bf16", "none", seed=8)
+    _, relu = run_tgemm(cuda_lib, M, N, K, "bf16", "relu", seed=8)
+    v = torch.from_numpy(none.view(np.int16)).view(torch.bfloat16).float()
+    want = torch.where(v > 0, v, torch.zeros_like(v)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(relu, want)
+    assert not (relu == 0x8000).any()
+
+
+def test_repeat_runs_are_deterministic(cuda_lib):
+    M, N, K = 1024, 1536, 2048
+    _, first = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=12)
+    for _ in range(5):
+        _, again = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=12)
+        assert np.array_equal(first, again)
+
+
+# ------------------------------------------------------------------ entry points
+def test_host_entry_point_matches_device_entry_point(cuda_lib):
+    M, N, K = 777, 1000, 520
+    (A, B, bias), dev = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=21)
+    Ah, Bh, bh = A.pin_memory(), B.pin_memory(), bias.pin_memory()
+    Ch = torch.full((M, N + 8), float("nan"), dtype=torch.float16).pin_memory()
+    Cv = Ch[:, :N]
+    cuda_lib.run_host(Ah, Bh, bh, Cv, "bias_relu")
+    torch.cuda.synchronize()
+    got = Ch.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got[:, :N], dev)
+    assert np.isnan(Ch[:, N:].float().numpy()).all()
+
+
+def test_host_memory_passed_to_device_entry_point_is_rejected(cuda_lib):
+    A = torch.ones((64, 64), dtype=torch.float16)
+    Cd = torch.empty((64, 64), dtype=torch.float16, device="cuda")
+    st = cuda_lib.tgemm_run(A.data_ptr(), A.data_ptr() + 64 * 64 * 2 * 4, 0, Cd.data_ptr(),
+                            64, 64, 64, 64, 64, 64, 0, 1, 0)
+    assert st == 1
+
+
+def test_no_kernel_timed_out(cuda_lib):
+    assert cuda_lib.tgemm_last_device_status() == 0
