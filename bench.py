@@ -76,9 +76,14 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling (every 20 ms) of SM clocks and throttle reasons.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Started before the load soak that precedes the timed region; mark() notes
+    when the timed region starts and ends, and summary() uses the samples taken
+    inside it (or, when the timed region is shorter than a few sampling
+    periods, those of the soak + timed window, and says so)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -86,17 +91,25 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.out = None
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         try:
             self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
         except OSError:
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -106,6 +119,16 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    @staticmethod
+    def _ts(text):
+        from datetime import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
     def summary(self):
         if self.proc is None or self.out is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -114,17 +137,25 @@ class ClockSampler:
         with open(self.out.name) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                if len(parts) >= 10 and parts[2].replace(".", "").isdigit():
                     rows.append(parts)
         os.unlink(self.out.name)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        sm = [float(r[1]) for r in rows]
+        inside = [r for r in rows if (t := self._ts(r[0])) is not None and self.t_start is not None
+                  and self.t_start <= t <= self.t_end]
+        window = "timed region"
+        if len(inside) < 3:
+            inside = [r for r in rows if (t := self._ts(r[0])) is not None and self.t_end is not None
+                      and t <= self.t_end] or rows
+            window = "load soak + timed region (timed region shorter than 3 samples)"
+        sm = [float(r[2]) for r in inside]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+        reasons = sorted({n for r in inside for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        pw = [float(r[4]) for r in inside if r[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(inside[0][3]),
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max(pw) if pw else None}
 
 
 def dist_setup():
@@ -159,7 +190,8 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 def cpu_oracle_sample(w, target_s: float):
-    """Time the fp64 oracle (as it stands) on a bounded sample of rows."""
+    """Time the fp64 oracle (as it stands) on a bounded sample of rows: the row
+    count grows until one run takes about target_s seconds (or covers all rows)."""
     import oracle
     A, B, bias = si.make_workload(w)
     ba, bb = si.bits(A), si.bits(B)
@@ -167,15 +199,14 @@ def cpu_oracle_sample(w, target_s: float):
     epi = si.EPILOGUES[w.epilogue]
     dt = oracle.dtype_code(w.dtype)
     cores = oracle.max_threads()
-    probe = list(range(min(w.M, max(cores, 1))))
-    t0 = time.perf_counter()
-    oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=probe)
-    t_probe = time.perf_counter() - t0
-    rows_n = int(max(len(probe), min(w.M, len(probe) * target_s / max(t_probe, 1e-6))))
-    rows = list(range(rows_n))
-    t0 = time.perf_counter()
-    oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=rows)
-    t = time.perf_counter() - t0
+    rows_n = min(w.M, max(cores, 1))
+    while True:
+        t0 = time.perf_counter()
+        oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=list(range(rows_n)))
+        t = time.perf_counter() - t0
+        if t >= 0.5 * target_s or rows_n >= w.M:
+            break
+        rows_n = int(min(w.M, max(rows_n * 2, rows_n * target_s / max(t, 1e-6))))
     return {"value": 2.0 * rows_n * w.N * w.K / t / 1e12, "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle", "seconds": round(t, 3),
             "sample": f"first {rows_n} of {w.M} rows of {w.name} (all {w.N} columns, K={w.K}), fp64"}
@@ -243,24 +274,33 @@ def run_tgemm_bench(args, world, rank, local):
     def step():
         tg.run(Ad, Bd, bd, Cd, w.epilogue, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
+    with torch.cuda.stream(stream), ClockSampler(local) as clk:
+        # Warm-up: at least W steps and at least args.soak seconds of them, so
+        # clocks and power settle before the timed region.
+        t_soak = time.perf_counter()
+        done = 0
+        while done < args.warmup or time.perf_counter() - t_soak < args.soak:
             flush.zero_()
             step()
+            done += 1
+            if done % 64 == 0:
+                torch.cuda.synchronize(dev)
         torch.cuda.synchronize(dev)
+        args.warmup_done = done
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         barrier(world)
         torch.cuda.synchronize(dev)
-        with ClockSampler(local) as clk:
-            t_wall = time.perf_counter()
-            for i in range(args.steps):
-                flush.zero_()
-                starts[i].record(stream)
-                step()
-                ends[i].record(stream)
-            torch.cuda.synchronize(dev)
-            t_wall = time.perf_counter() - t_wall
+        clk.mark_start()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+        clk.mark_end()
         barrier(world)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     mean_ms = sum(launch_ms) / len(launch_ms)
@@ -302,7 +342,7 @@ def run_tgemm_bench(args, world, rank, local):
     achieved = flops / (mean_ms * 1e-3) / 1e12
     traffic = recorded_traffic(args.config)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms_max,
+            "steps": args.steps, "warmup": args.warmup_done, "ms_per_step": mean_ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic", "config": workload_config(w),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -325,13 +365,14 @@ def run_tgemm_bench(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tgemm", "reference"], default="tgemm")
     ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--soak", type=float, default=1.0, help="minimum seconds of warm-up steps")
     ap.add_argument("--ref-rows", type=int, default=64, help="oracle rows per reference step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)          # at least 3 untimed warm-up steps

@@ -22,8 +22,9 @@
 //   warps 2..5  epilogue: tcgen05.ld TMEM -> registers (each warp owns the 32
 //               TMEM lanes = 32 rows its warp index allows), + bias, ReLU,
 //               round to fp16/bf16, 128B-swizzled staging in shared memory,
-//               then a TMA store (clipped at ragged M/N edges) or, when C's
-//               pitch is not 16-byte aligned, masked coalesced stores.
+//               then a TMA store (clipped at the ragged M edge) or masked
+//               coalesced stores (a chunk crossing the ragged N edge, or a C
+//               pitch that is not 16-byte aligned).
 //
 // Tiles are visited in a grouped order (GROUP_M row-blocks per column sweep,
 // the L2 block swizzle of T.use_swizzle) by a persistent grid of at most one
@@ -340,6 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Stage the 32 x 64 block: row `lane`, 16-byte chunk j at (j ^ (lane & 7)).
                 const uint32_t sb = cstage0 + buf * kCStageBytes;
                 uint8_t *sb_gen = cstage_gen0 + buf * kCStageBytes;
+                // A TMA store clips the ragged column edge only at 16-byte
+                // granularity, so a chunk that crosses N takes the masked path.
+                const bool use_tma = p.tma_store && (n0 + 64 <= p.N);
                 if (p.tma_store && lane == 0) bulk_wait_group_read<1>();   // buffer reused 2 stores later
                 __syncwarp();
 #pragma unroll
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  "r"(packed[4 * j + 3])
                                  : "memory");
                 }
-                if (p.tma_store) {
+                if (use_tma) {
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {

@@ -19,7 +19,7 @@ import torch
 import oracle
 import seeded_inputs as si
 from gpu_helpers import (EPI, assert_bit_exact, assert_close, assert_pad_untouched, c_bits,
-                         oracle_ref, run_tgemm)
+                         magnitude, oracle_ref, run_tgemm)
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ def test_workload_full_size(cuda_lib, name):
     assert_pad_untouched(got, w.N, name)
     rows = list(range(w.M)) if w.M * w.N * w.K <= 2 ** 26 else sample_rows(w.M, seed=w.seed)
     ref = oracle_ref(inputs, w.M, w.N, w.K, w.dtype, w.epilogue, rows=rows)
-    assert_close(got[rows, : w.N], ref, w.dtype, name)
+    assert_close(got[rows, : w.N], ref, w.dtype, name, magnitude(inputs, w.N, w.K, rows), w.K)
     del ldc
 
 
@@ -82,7 +82,7 @@ def test_small_and_odd_shapes(cuda_lib, M, N, K):
     assert_bit_exact(got, ref, dtype, f"{M}x{N}x{K} {epi} {dtype}")
     inputs, got = run_tgemm(cuda_lib, M, N, K, dtype, epi, seed=idx)
     ref = oracle_ref(inputs, M, N, K, dtype, epi)
-    assert_close(got, ref, dtype, f"{M}x{N}x{K} {epi} {dtype}")
+    assert_close(got, ref, dtype, f"{M}x{N}x{K} {epi} {dtype}", magnitude(inputs, N, K), K)
 
 
 @pytest.mark.parametrize("bn", ["64", "128", "256"])
@@ -96,7 +96,8 @@ def test_each_tile_config_epilogue_dtype(cuda_lib, monkeypatch, bn, dtype, epi):
     inputs, got = run_tgemm(cuda_lib, M, N, K, dtype, epi, seed=5, kind="int")
     assert_bit_exact(got, oracle_ref(inputs, M, N, K, dtype, epi), dtype, f"int bn={bn}")
     inputs, got = run_tgemm(cuda_lib, M, N, K, dtype, epi, seed=6)
-    assert_close(got, oracle_ref(inputs, M, N, K, dtype, epi), dtype, f"bn={bn}")
+    assert_close(got, oracle_ref(inputs, M, N, K, dtype, epi), dtype, f"bn={bn}",
+                 magnitude(inputs, N, K), K)
 
 
 @pytest.mark.parametrize("bn", ["64", "128", "256"])
