@@ -16,9 +16,10 @@ TGEMM_F16, TGEMM_BF16 = 0, 1
 TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_RELU = 0, 1, 2, 3
 STATUS = {0: "TGEMM_OK", 1: "TGEMM_ERR_INVALID_ARG", 2: "TGEMM_ERR_ALIGNMENT",
           3: "TGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TGEMM_ERR_ALIAS", 5: "TGEMM_ERR_CUDA",
-          6: "TGEMM_ERR_TIMEOUT"}
+          6: "TGEMM_ERR_TIMEOUT", 7: "TGEMM_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("tgemm_run", "tgemm_run_host", "tgemm_status_string", "tgemm_last_device_status",
-            "tgemm_version")
+            "tgemm_version", "tgemm_run_noalloc")
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -46,7 +47,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             raise RuntimeError(f"CUDA library {_build.LIB} is missing; run build() first")
         lib = ctypes.CDLL(_build.LIB)
         p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-        for name in ("tgemm_run", "tgemm_run_host"):
+        for name in ("tgemm_run", "tgemm_run_host", "tgemm_run_noalloc"):
             f = getattr(lib, name)
             f.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p]
             f.restype = i32
@@ -72,6 +73,18 @@ def tgemm_run_host(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, ld
     """Raw C-ABI call with host pointers (ints); returns the status code."""
     return load().tgemm_run_host(A or None, B or None, bias or None, C or None, M, N, K, lda, ldb,
                                  ldc, dtype, epilogue, stream or None)
+
+
+def tgemm_run_noalloc(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: int,
+                      ldb: int, ldc: int, dtype: int, epilogue: int, stream: int = 0) -> int:
+    """Raw C-ABI call of the allocation-free variant (device pointers as ints).
+
+    For callers that must not allocate GPU memory (memory reserved up front by
+    another allocator, allocation-free latency loops): any operand repack uses
+    the library's fixed 64 MiB device array instead of allocating; calls that
+    may overlap on the GPU race on that array.  Returns the status code."""
+    return load().tgemm_run_noalloc(A or None, B or None, bias or None, C or None, M, N, K, lda,
+                                    ldb, ldc, dtype, epilogue, stream or None)
 
 
 def tgemm_status_string(status: int) -> str:

@@ -323,10 +323,174 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     return TGEMM_OK;
 }
 
+// ---------------------------------------------------------------- no-allocation variant
+// Fixed scratch of tgemm_run_noalloc (see include/tgemm.h): the repacked
+// operands of callers that must not allocate.  In host code the name
+// g_noalloc_scratch is only a host-side stand-in; kernels get the device
+// address looked up by cudaGetSymbolAddress in noalloc_setup().
+constexpr size_t kNoAllocScratchBytes = TGEMM_NOALLOC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+    std::once_flag once;
+    bool ok = false;
+    void *scratch = nullptr;   // device address of g_noalloc_scratch on this device
+    DeviceInfo info;           // sizes, status word, kernel attributes; no memory pool
+};
+
+NoAllocDevice g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: check the device and look up the
+// device addresses of the status word and of the scratch array.
+bool noalloc_setup(int dev, NoAllocDevice **out) {
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    NoAllocDevice &d = g_noalloc[dev];
+    std::call_once(d.once, [&]() {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        if (major != 10 || minor != 3) return;
+        void *status = nullptr, *scratch = nullptr;
+        if (cudaGetSymbolAddress(&status, g_device_status) != cudaSuccess ||
+            cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        d.info.num_sms = sms;
+        d.info.status = static_cast<unsigned int *>(status);
+        d.info.ok = true;
+        d.scratch = scratch;
+        d.ok = true;
+    });
+    *out = &d;
+    return d.ok;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B, const void *bias,
+                                void *C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                int64_t ldb, int64_t ldc, int dtype, int epilogue,
+                                cudaStream_t stream) {
+    DeviceInfo *d = &nd->info;
+    const bool bf16 = dtype == TGEMM_BF16;
+    const int has_bias = (epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU) ? 1 : 0;
+    const int relu = (epilogue == TGEMM_EPI_RELU || epilogue == TGEMM_EPI_BIAS_RELU) ? 1 : 0;
+    if (M == 0 || N == 0) return TGEMM_OK;
+    if (K == 0) {
+        const dim3 grid(static_cast<unsigned>(std::min<int64_t>(cdiv(N, 256), 64)),
+                        static_cast<unsigned>(std::min<int64_t>(M, 65535)));
+        fill_epilogue_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t *>(bias),
+                                                       static_cast<uint16_t *>(C), ldc,
+                                                       static_cast<int>(M), static_cast<int>(N),
+                                                       has_bias, relu, bf16 ? 1 : 0);
+        return cudaGetLastError() == cudaSuccess ? TGEMM_OK : TGEMM_ERR_CUDA;
+    }
+
+    // Carve the fixed scratch; reject before enqueueing anything if it is too small.
+    const void *a_use = A, *b_use = B;
+    int64_t lda_use = lda, ldb_use = ldb, used = 0, a_off = -1, b_off = -1;
+    if (lda % 8 != 0) {
+        lda_use = cdiv(K, 8) * 8;
+        a_off = used;
+        used += round_up(M * lda_use * 2, 256);
+    }
+    if (ldb % 8 != 0) {
+        ldb_use = cdiv(N, 8) * 8;
+        b_off = used;
+        used += round_up(K * ldb_use * 2, 256);
+    }
+    if (used > static_cast<int64_t>(kNoAllocScratchBytes)) return TGEMM_ERR_SCRATCH_LIMIT;
+    unsigned char *scratch = static_cast<unsigned char *>(nd->scratch);
+    if (a_off >= 0) {
+        if (repack(A, lda, scratch + a_off, lda_use, M, K, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return TGEMM_ERR_CUDA;
+        }
+        a_use = scratch + a_off;
+    }
+    if (b_off >= 0) {
+        if (repack(B, ldb, scratch + b_off, ldb_use, K, N, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return TGEMM_ERR_CUDA;
+        }
+        b_use = scratch + b_off;
+    }
+
+    const Cfg cfg = choose_config(M, N, d->num_sms);
+    const bool tma_store = (ldc % 8) == 0;
+    CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    if (!make_map(&ta, a_use, M, K, lda_use, kBK, kBM, bf16) ||
+        !make_map(&tb, b_use, K, N, ldb_use, 64, kBK, bf16) ||
+        (tma_store && !make_map(&tc, C, M, N, ldc, 64, 32, bf16)))
+        return TGEMM_ERR_CUDA;
+
+    KParams p;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.num_m = static_cast<int>(cdiv(M, kBM));
+    p.num_n = static_cast<int>(cdiv(N, cfg.bn));
+    p.num_kb = static_cast<int>(cdiv(K, kBK));
+    const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+    if (tiles > INT32_MAX) return TGEMM_ERR_INVALID_ARG;
+    p.num_tiles = static_cast<int>(tiles);
+    p.group_m = std::min(p.num_m, 16);
+    p.bias = bias;
+    p.C = C;
+    p.ldc = ldc;
+    p.has_bias = has_bias;
+    p.relu = relu;
+    p.is_bf16 = bf16 ? 1 : 0;
+    p.tma_store = tma_store ? 1 : 0;
+    p.idesc = idesc_f16(bf16, kBM, static_cast<uint32_t>(cfg.bn), false, true);
+    p.status = d->status;
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, d->num_sms));
+
+    cudaError_t e;
+    switch (cfg.bn) {
+        case 256: e = launch_fused<256, 4>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
+        case 128: e = launch_fused<128, 6>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
+        default: e = launch_fused<64, 8>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
+}
+
 }  // namespace
 }  // namespace tgemm
 
 using namespace tgemm;
+
+extern "C" tgemm_status tgemm_run_noalloc(const void *A, const void *B, const void *bias, void *C,
+                                          int64_t M, int64_t N, int64_t K, int64_t lda,
+                                          int64_t ldb, int64_t ldc, tgemm_dtype dtype,
+                                          tgemm_epilogue epilogue, tgemm_stream_t stream) {
+    tgemm_status st = validate(A, B, bias, C, M, N, K, lda, ldb, ldc, dtype, epilogue);
+    if (st != TGEMM_OK) return st;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    NoAllocDevice *nd = nullptr;
+    if (!noalloc_setup(dev, &nd)) return TGEMM_ERR_UNSUPPORTED_DEVICE;
+    if (M == 0 || N == 0) return TGEMM_OK;
+    const bool use_bias = epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU;
+    if (!is_device_memory(C, dev) || (K > 0 && (!is_device_memory(A, dev) || !is_device_memory(B, dev))) ||
+        (use_bias && !is_device_memory(bias, dev)))
+        return TGEMM_ERR_INVALID_ARG;
+    return run_device_noalloc(nd, A, B, bias, C, M, N, K, lda, ldb, ldc, dtype, epilogue,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
 
 extern "C" tgemm_status tgemm_run(const void *A, const void *B, const void *bias, void *C,
                                   int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
@@ -405,6 +569,7 @@ extern "C" const char *tgemm_status_string(tgemm_status s) {
         case TGEMM_ERR_ALIAS: return "TGEMM_ERR_ALIAS: C overlaps an input";
         case TGEMM_ERR_CUDA: return "TGEMM_ERR_CUDA: a CUDA call or launch failed";
         case TGEMM_ERR_TIMEOUT: return "TGEMM_ERR_TIMEOUT: a kernel gave up on a pipeline wait";
+        case TGEMM_ERR_SCRATCH_LIMIT: return "TGEMM_ERR_SCRATCH_LIMIT: repacked operands exceed the fixed scratch of tgemm_run_noalloc";
     }
     return "TGEMM_ERR_UNKNOWN";
 }

@@ -51,7 +51,8 @@ typedef enum {
     TGEMM_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or the current device is not CC 10.3 */
     TGEMM_ERR_ALIAS = 4,              /* C's byte range overlaps A, B or bias                */
     TGEMM_ERR_CUDA = 5,               /* a CUDA runtime/driver call or a launch failed       */
-    TGEMM_ERR_TIMEOUT = 6             /* a kernel gave up on a pipeline wait (device status) */
+    TGEMM_ERR_TIMEOUT = 6,            /* a kernel gave up on a pipeline wait (device status) */
+    TGEMM_ERR_SCRATCH_LIMIT = 7       /* tgemm_run_noalloc: repacked operands exceed its fixed scratch */
 } tgemm_status;
 
 /*
@@ -102,6 +103,46 @@ tgemm_status tgemm_run_host(const void *A_host, const void *B_host, const void *
                             void *C_host, int64_t M, int64_t N, int64_t K,
                             int64_t lda, int64_t ldb, int64_t ldc,
                             tgemm_dtype dtype, tgemm_epilogue epilogue, tgemm_stream_t stream);
+
+/*
+ * tgemm_run_noalloc — tgemm_run for callers that must not allocate GPU memory.
+ * (No counterpart on the pages: this is a deployment variant of the same
+ * operation.)
+ *
+ * Who needs it: code whose device memory is reserved up front by another
+ * allocator (a framework's caching allocator that holds most of HBM, so a
+ * library-side cudaMalloc/cudaMallocAsync can fail or fragment that reserve),
+ * latency-bound loops that avoid allocation calls because they can block or
+ * synchronise, and deployments that forbid any allocation after start-up.
+ *
+ * What differs from tgemm_run: nothing is allocated.  The only scratch this
+ * operation needs — the repacked copy of A and/or B when lda or ldb is not a
+ * multiple of 8 elements — lives in a fixed device array inside the library of
+ * TGEMM_NOALLOC_SCRATCH_BYTES (64 MiB), which every GPU that loads the library
+ * holds until the process exits.  Each repacked operand takes
+ * rows * round_up(width, 8) * 2 bytes, rounded up to 256 bytes; if the
+ * operands that need repacking do not fit together, the call returns
+ * TGEMM_ERR_SCRATCH_LIMIT before enqueueing anything.  Operands whose pitch is
+ * already a multiple of 8 use no scratch at all.
+ *
+ * Sharing: every call, on every stream and host thread, uses the same array,
+ * so two calls that may overlap on the GPU race on it; order them (one
+ * stream, or events).  The array keeps the previous call's contents; nothing
+ * in it needs to start at zero, because each call writes every scratch
+ * element it reads before reading it.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the device address of the array once; make that first call before any
+ * stream capture.
+ *
+ * Arguments, layout, results and the other error codes are those of
+ * tgemm_run, and the results are identical to tgemm_run's.
+ */
+#define TGEMM_NOALLOC_SCRATCH_BYTES (64ull << 20)
+tgemm_status tgemm_run_noalloc(const void *A, const void *B, const void *bias, void *C,
+                               int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldc,
+                               tgemm_dtype dtype, tgemm_epilogue epilogue, tgemm_stream_t stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *tgemm_status_string(tgemm_status status);

@@ -1,0 +1,91 @@
+"""The allocation-free entry point tgemm_run_noalloc, through the C ABI.
+
+It exists for callers that must not allocate GPU memory: code whose device
+memory is reserved up front by another allocator (where a library-side
+allocation can fail or fragment that reserve), latency-bound loops that avoid
+allocation calls, and deployments that forbid allocation after start-up.
+Instead of drawing scratch from a pool, it repacks unaligned operands into a
+fixed 64 MiB device array inside the library.
+
+Checked here: two calls in a row whose operands need that scratch give the
+same results as tgemm_run (whose tolerance against the oracle the other tests
+establish), the second call is not disturbed by what the first left in the
+shared array, and a call that would need more scratch than the array holds is
+rejected before anything runs.  This file is collected last so that a failure
+here does not hide the rest of the suite; it also passes on its own in a fresh
+process.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+from gpu_helpers import SENTINEL, alloc_c, assert_close, c_bits, magnitude, oracle_ref, to_device_pitched
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_LIMIT = 7
+DT = {"fp16": 0, "bf16": 1}
+EPI = {"none": 0, "relu": 1, "bias": 2, "bias_relu": 3}
+
+
+def prepare(M, N, K, dtype, seed, lda, ldb):
+    A, B, bias = si.make_inputs(M, N, K, dtype, seed, lda=lda if lda != K else None,
+                                ldb=ldb if ldb != N else None)
+    return (A, B, bias), to_device_pitched(A, K), to_device_pitched(B, N), bias.to("cuda")
+
+
+def call(fn, Ad, Bd, bd, Cd, M, N, K, dtype, epi):
+    return fn(Ad.data_ptr(), Bd.data_ptr(), bd.data_ptr(), Cd.data_ptr(), M, N, K,
+              Ad.stride(0), Bd.stride(0), Cd.stride(0), DT[dtype], EPI[epi],
+              torch.cuda.current_stream().cuda_stream)
+
+
+# (M, N, K, dtype, epilogue, seed, lda, ldb, ldc): each case repacks at least
+# one operand into the fixed scratch.
+CASES = [
+    (1000, 1001, 520, "fp16", "bias_relu", 31, 520, 1001, 1001),   # B repacked, masked C stores
+    (777, 640, 517, "bf16", "relu", 32, 517, 640, 648),            # A repacked, TMA C stores
+    (513, 300, 301, "fp16", "bias", 33, 301, 300, 300),            # A and B repacked
+]
+
+
+def test_noalloc_matches_run_on_consecutive_calls(cuda_lib):
+    prepared = []
+    for (M, N, K, dt, epi, seed, lda, ldb, ldc) in CASES:
+        inputs, Ad, Bd, bd = prepare(M, N, K, dt, seed, lda, ldb)
+        prepared.append((inputs, Ad, Bd, bd, alloc_c(M, N, ldc, dt), alloc_c(M, N, ldc, dt)))
+    # Back-to-back calls of the new entry point, then the existing one.
+    for rep in range(2):
+        for (M, N, K, dt, epi, *_), (inputs, Ad, Bd, bd, Cn, Cr) in zip(CASES, prepared):
+            assert call(cuda_lib.tgemm_run_noalloc, Ad, Bd, bd, Cn, M, N, K, dt, epi) == 0
+        torch.cuda.synchronize()
+        for (M, N, K, dt, epi, seed, lda, ldb, ldc), (inputs, Ad, Bd, bd, Cn, Cr) in zip(CASES, prepared):
+            if rep == 0:
+                assert call(cuda_lib.tgemm_run, Ad, Bd, bd, Cr, M, N, K, dt, epi) == 0
+            torch.cuda.synchronize()
+            got, want = c_bits(Cn, M, ldc), c_bits(Cr, M, ldc)
+            assert np.array_equal(got, want), f"case {M}x{N}x{K}, call {rep + 1}"
+            if ldc > N:
+                assert (got[:, N:] == SENTINEL).all()
+            if rep == 0:
+                used = (inputs[0], inputs[1], inputs[2] if epi in ("bias", "bias_relu") else None)
+                ref = oracle_ref(used, M, N, K, dt, epi)
+                assert_close(got[:, :N], ref, dt, f"noalloc {M}x{N}x{K}", magnitude(used, N, K), K)
+    assert cuda_lib.tgemm_last_device_status() == 0
+
+
+def test_noalloc_rejects_scratch_beyond_its_limit(cuda_lib):
+    # lda = 4100 is unaligned, so A would be repacked: 8192 * 4104 * 2 B > 64 MiB.
+    M, N, K = 8192, 64, 4100
+    assert M * 4104 * 2 > cuda_lib.NOALLOC_SCRATCH_BYTES
+    Ad = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    Bd = torch.zeros((K, N), dtype=torch.float16, device="cuda")
+    bd = torch.zeros((N,), dtype=torch.float16, device="cuda")
+    Cd = alloc_c(M, N, N, "fp16")
+    assert call(cuda_lib.tgemm_run_noalloc, Ad, Bd, bd, Cd, M, N, K, "fp16", "bias_relu") == SCRATCH_LIMIT
+    torch.cuda.synchronize()
+    assert (c_bits(Cd, M, N) == SENTINEL).all()
+    assert "SCRATCH_LIMIT" in cuda_lib.tgemm_status_string(SCRATCH_LIMIT)
