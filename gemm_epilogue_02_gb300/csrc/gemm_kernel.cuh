@@ -9,22 +9,31 @@
 // §10.8 / "TileLang で GPU カーネル設計を解説" §4 (bias indexed by the output
 // column, added to the fp32 accumulator before the activation, one rounding at
 // the store), laid out for sm_103a instead of the pages' register-fragment
-// design:
+// design.
 //
-//   warp 0      TMA producer: A tile [128 x 64] (K-major) and B tile [64 x BN]
-//               (N-major, as BN/64 sub-tiles of 64 columns) per k-block into a
-//               STAGES-deep shared-memory ring, 128-byte swizzled; full/empty
-//               mbarriers per stage (the software pipeline of T.Pipelined).
-//   warp 1      allocates TMEM (two BN-column fp32 accumulators) and one lane
-//               issues tcgen05.mma (M=128, N=BN, K=16) per 16-wide k step; a
-//               tcgen05.commit frees each ring stage and publishes each
-//               finished accumulator.
+// A work unit ("tile") is (128 * CG) rows x BN columns of C, computed by a
+// group of CG CTAs (CG = 1: one CTA; CG = 2: a cluster pair whose MMAs span
+// both SMs, M = 256).  In every CTA:
+//
+//   warp 0      TMA producer: its own 128 rows of A [128 x 64] (K-major) and
+//               its BN/CG columns of B [64 x BN/CG] (N-major, as sub-tiles of
+//               64 columns) per k-block into a STAGES-deep shared-memory ring,
+//               128-byte swizzled.  The stage's full barrier lives in CTA rank 0
+//               and counts the bytes of both CTAs (rank 0 announces them all;
+//               the peer's copies report there); each CTA's empty barrier is
+//               released by the MMA's commit (the software pipeline of
+//               T.Pipelined).
+//   warp 1      allocates TMEM (two BN-column fp32 accumulators); in rank 0 one
+//               lane issues tcgen05.mma (M = 128*CG, N = BN, K = 16) per 16-wide
+//               k step; a tcgen05.commit frees each ring stage (in both CTAs)
+//               and publishes each finished accumulator (to both CTAs).
 //   warps 2..5  epilogue: tcgen05.ld TMEM -> registers (each warp owns the 32
 //               TMEM lanes = 32 rows its warp index allows), + bias, ReLU,
 //               round to fp16/bf16, 128B-swizzled staging in shared memory,
 //               then a TMA store (clipped at the ragged M edge) or masked
 //               coalesced stores (a chunk crossing the ragged N edge, or a C
-//               pitch that is not 16-byte aligned).
+//               pitch that is not 16-byte aligned).  The accumulator is handed
+//               back to rank 0's MMA lane right after its last read.
 //
 // Tiles are visited in a grouped order (GROUP_M row-blocks per column sweep,
 // the L2 block swizzle of T.use_swizzle) by a persistent grid of at most one
@@ -43,13 +52,14 @@
 
 namespace tgemm {
 
-constexpr int kBM = 128;          // rows per tile (TMEM lanes)
+constexpr int kBM = 128;          // rows per CTA (TMEM lanes)
 constexpr int kBK = 64;           // k per ring stage: 64 x 2 B = one 128-byte swizzle row
 constexpr int kUmmaK = 16;        // k per tcgen05.mma (kind::f16)
 constexpr int kThreads = 192;     // 6 warps
 constexpr int kEpiWarps = 4;
 constexpr uint32_t kCStageBytes = 32 * 128;   // 32 rows x 64 columns x 2 B
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kPeerCopyGraceNs = 200000ull;   // 200 us for in-flight copies on abort
 constexpr uint32_t kStatusTimeout = 6;             // TGEMM_ERR_TIMEOUT
 
 struct KParams {
@@ -63,11 +73,12 @@ struct KParams {
     unsigned int *status;      // device status word
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 struct Smem {
+    static constexpr int kBCols = BN / CG;                      // columns of B per CTA
     static constexpr uint32_t kABytes = kBM * kBK * 2;          // 16 KiB
-    static constexpr uint32_t kBBytes = kBK * BN * 2;           // BN/64 sub-tiles of 8 KiB
-    static constexpr uint32_t kStageTx = kABytes + kBBytes;
+    static constexpr uint32_t kBBytes = kBK * kBCols * 2;       // kBCols/64 sub-tiles of 8 KiB
+    static constexpr uint32_t kStageTx = kABytes + kBBytes;     // bytes one CTA loads per stage
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
     static constexpr uint32_t kOffC = kOffB + STAGES * kBBytes;
@@ -80,6 +91,9 @@ struct Smem {
     static constexpr uint32_t kDynamicBytes = kBytes + 1024;   // 1 KiB alignment slack
     static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
                                           : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
+    static_assert(kBCols % 64 == 0, "B is loaded in 64-column sub-tiles");
+    static_assert(2 * BN <= 512, "two accumulators must fit in TMEM");
     static_assert(kDynamicBytes <= 232448, "shared memory budget exceeded");
     static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "swizzled buffers need 1 KiB alignment");
 };
@@ -139,11 +153,11 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CG>
 __global__ void __launch_bounds__(kThreads, 1)
     tgemm_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const KParams p) {
-    using L = Smem<BN, STAGES>;
+    using L = Smem<BN, STAGES, CG>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -159,15 +173,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const int group_id = (CG == 2) ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int num_groups = (CG == 2) ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
+    // Barriers that rank 0 owns for the whole group, as shared::cluster addresses.
+    auto leader_full = [&](int s) { return (CG == 2) ? mapa_shared(full_bar(s), 0) : full_bar(s); };
+    auto leader_tempty = [&](int a) { return (CG == 2) ? mapa_shared(tempty_bar(a), 0) : tempty_bar(a); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), 1);             // rank 0's expect-tx arrival (bytes of the whole group)
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), kEpiWarps);
+            mbar_init(tempty_bar(a), kEpiWarps * CG);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -179,9 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmB);
         if (p.tma_store) prefetch_tmap(&tmC);
     }
+    if constexpr (CG == 2) cluster_sync();       // the peer is running and its barriers exist
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_u32(tmem_holder), L::kTmemCols);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
     __syncthreads();
@@ -196,38 +217,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t uses[STAGES];
             for (int s = 0; s < STAGES; ++s) uses[s] = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            for (int t = group_id; t < p.num_tiles && ok; t += num_groups) {
                 int m_blk, n_blk;
                 tile_coords(t, p, m_blk, n_blk);
+                const int a_row = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM;
+                const int b_col = n_blk * BN + static_cast<int>(rank) * L::kBCols;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, L::kStageTx);
                     const uint32_t a_dst = sbase + L::kOffA + stage * L::kABytes;
                     const uint32_t b_dst = sbase + L::kOffB + stage * L::kBBytes;
-                    tma_load_2d(a_dst, &tmA, fb, kb * kBK, m_blk * kBM);
+                    if constexpr (CG == 1) {
+                        const uint32_t fb = full_bar(stage);
+                        mbar_arrive_expect_tx(fb, L::kStageTx);
+                        tma_load_2d(a_dst, &tmA, fb, kb * kBK, a_row);
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(b_dst + j * (kBK * 128), &tmB, fb, n_blk * BN + j * 64, kb * kBK);
+                        for (int j = 0; j < L::kBCols / 64; ++j)
+                            tma_load_2d(b_dst + j * (kBK * 128), &tmB, fb, b_col + j * 64, kb * kBK);
+                    } else {
+                        // Rank 0 announces the bytes of both CTAs; the peer's copies
+                        // report to rank 0's barrier (its transaction count may dip
+                        // below zero until the announcement lands, which is allowed).
+                        const uint32_t fb = leader_full(stage);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), CG * L::kStageTx);
+                        tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, a_row);
+#pragma unroll
+                        for (int j = 0; j < L::kBCols / 64; ++j)
+                            tma_load_2d_pair(b_dst + j * (kBK * 128), &tmB, fb, b_col + j * 64, kb * kBK);
+                    }
                     ++uses[stage];
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
             if (!ok) {
                 // Let every copy this thread started land before the CTA exits.
-                for (int s = 0; s < STAGES; ++s)
-                    if (uses[s]) drain_wait(full_bar(s), (uses[s] - 1u) & 1u);
+                if (CG == 1 || rank == 0) {
+                    for (int s = 0; s < STAGES; ++s)
+                        if (uses[s]) drain_wait(full_bar(s), (uses[s] - 1u) & 1u);
+                } else {
+                    // The peer's copies report to rank 0's barriers: give them time to land.
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < kPeerCopyGraceNs) {
+                    }
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            for (int t = group_id; t < p.num_tiles && ok; t += num_groups) {
                 if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -243,17 +285,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // B: N-major; 64-column sub-tiles kBK*128 B apart (leading), 8-row k groups
                         // 1 KiB apart (stride); a 16-wide k step is 16 rows = 2 KiB.
                         const uint64_t bdesc = sw128_desc(b_addr + k * (kUmmaK * 128), kBK * 128, 1024);
-                        mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_ss<CG>(d_tmem, adesc, bdesc, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    mma_commit(empty_bar(stage));          // frees the ring stage once read
+                    mma_commit<CG>(empty_bar(stage));      // frees the ring stage once read
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit(tfull_bar(acc));                // accumulator ready for the epilogue
+                mma_commit<CG>(tfull_bar(acc));            // accumulator ready for the epilogue
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             // All MMAs issued by this thread complete before TMEM is released.
-            mma_commit(drain_bar);
+            mma_commit_local<CG>(drain_bar);
             drain_wait(drain_bar, 0);
         }
     } else {
@@ -265,7 +307,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         int buf = 0;
         const uint32_t cstage0 = sbase + L::kOffC + ew * 2 * kCStageBytes;
         uint8_t *cstage_gen0 = smem + L::kOffC + ew * 2 * kCStageBytes;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        auto release_acc = [&](int a) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 1) mbar_arrive(tempty_bar(a));
+                else mbar_arrive_cluster(leader_tempty(a));
+            }
+        };
+        for (int t = group_id; t < p.num_tiles; t += num_groups) {
             int m_blk, n_blk;
             tile_coords(t, p, m_blk, n_blk);
             int ok = 1;
@@ -273,16 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const int m0 = m_blk * kBM + q * 32;
+            const int m0 = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM + q * 32;
             const int n_tile = n_blk * BN;
             // Only chunks / rows that intersect C are read out and stored (no
             // store is ever issued at a coordinate outside the tensor).
             const int c_end = (m0 < p.M) ? min(BN / 64, (p.N - n_tile + 63) / 64) : 0;
-            if (c_end == 0) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(acc));
-            }
+            if (c_end == 0) release_acc(acc);
 #pragma unroll 1
             for (int c = 0; c < c_end; ++c) {
                 uint32_t r[64];
@@ -291,12 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
                 tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
                 tmem_wait_ld();
-                if (c == c_end - 1) {
-                    // Last read of this accumulator: hand it back to the MMA warp.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty_bar(acc));
-                }
+                // Last read of this accumulator: hand it back to the MMA lane.
+                if (c == c_end - 1) release_acc(acc);
                 const int n0 = n_tile + c * 64;
                 uint32_t packed[32];
                 const bool full_bias = p.has_bias && (n0 + 64 <= p.N);
@@ -388,8 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2) cluster_sync();       // both CTAs are done with TMEM and remote barriers
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, L::kTmemCols);
+    if (warp == 1) tmem_dealloc<CG>(tmem_base, L::kTmemCols);
+    if constexpr (CG == 2) cluster_sync();       // the peer stays resident until both have freed TMEM
 }
 
 }  // namespace tgemm

@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <string>
 
 #include "../../include/tgemm.h"
 #include "aux_kernels.cuh"
@@ -33,6 +34,7 @@ struct DeviceInfo {
     cudaMemPool_t pool = nullptr;
     std::mutex mu;          // guards lazily set kernel attributes
     unsigned attr_set = 0;  // bit per kernel configuration
+    int max_clusters[3] = {0, 0, 0};   // co-resident clusters per CTA-group size
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -173,46 +175,114 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int6
 }
 
 // ---------------------------------------------------------------- configs
+// A configuration: C tile = (128 * cg) x bn, `stages` ring stages, cg CTAs per tile.
 struct Cfg {
     int bn;
     int stages;
+    int cg;
     int bit;
 };
-constexpr Cfg kCfg256 = {256, 4, 1};
-constexpr Cfg kCfg128 = {128, 6, 2};
-constexpr Cfg kCfg64 = {64, 8, 4};
+constexpr Cfg kCfg256 = {256, 4, 1, 1};
+constexpr Cfg kCfg128 = {128, 6, 1, 2};
+constexpr Cfg kCfg64 = {64, 8, 1, 4};
+constexpr Cfg kCfg256x2 = {256, 6, 2, 8};
+constexpr Cfg kCfg128x2 = {128, 8, 2, 16};
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 Cfg choose_config(int64_t M, int64_t N, int num_sms) {
-    if (const char *f = std::getenv("TGEMM_FORCE_BN")) {
-        const int bn = std::atoi(f);
-        if (bn == 256) return kCfg256;
-        if (bn == 128) return kCfg128;
-        if (bn == 64) return kCfg64;
+    if (const char *f = std::getenv("TGEMM_FORCE_CFG")) {
+        const std::string v(f);
+        if (v == "256") return kCfg256;
+        if (v == "128") return kCfg128;
+        if (v == "64") return kCfg64;
+        if (v == "256x2") return kCfg256x2;
+        if (v == "128x2") return kCfg128x2;
     }
+    // A CTA pair (256-row tiles) halves the B operand each SM stages; use it
+    // when the pair tiles still give every SM pair work.
+    if (M > kBM && cdiv(M, 2 * kBM) * cdiv(N, 256) >= num_sms / 2) return kCfg256x2;
     const int64_t mt = cdiv(M, kBM);
     if (mt * cdiv(N, 256) >= num_sms) return kCfg256;
     if (mt * cdiv(N, 128) >= num_sms) return kCfg128;
     return kCfg64;
 }
 
-template <int BN, int ST>
+template <int BN, int ST, int CG>
 cudaError_t launch_fused(DeviceInfo *d, int bit, const CUtensorMap &ta, const CUtensorMap &tb,
-                         const CUtensorMap &tc, const KParams &p, int grid, cudaStream_t s) {
-    using L = Smem<BN, ST>;
+                         const CUtensorMap &tc, const KParams &p, int64_t tiles, cudaStream_t s) {
+    using L = Smem<BN, ST, CG>;
+    auto kernel = tgemm_fused_kernel<BN, ST, CG>;
+    int max_groups = d->num_sms;
     {
         std::lock_guard<std::mutex> g(d->mu);
         if (!(d->attr_set & bit)) {
-            cudaError_t e = cudaFuncSetAttribute(tgemm_fused_kernel<BN, ST>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  L::kDynamicBytes);
             if (e != cudaSuccess) return e;
+            if (CG == 2) {
+                cudaLaunchConfig_t qc;
+                std::memset(&qc, 0, sizeof(qc));
+                cudaLaunchAttribute qa[1];
+                qa[0].id = cudaLaunchAttributeClusterDimension;
+                qa[0].val.clusterDim.x = CG;
+                qa[0].val.clusterDim.y = 1;
+                qa[0].val.clusterDim.z = 1;
+                qc.gridDim = dim3(CG * (d->num_sms / CG));
+                qc.blockDim = dim3(kThreads);
+                qc.dynamicSmemBytes = L::kDynamicBytes;
+                qc.attrs = qa;
+                qc.numAttrs = 1;
+                int clusters = 0;
+                if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &qc) != cudaSuccess || clusters <= 0) {
+                    cudaGetLastError();
+                    clusters = d->num_sms / CG;
+                }
+                d->max_clusters[CG] = clusters;
+            }
             d->attr_set |= bit;
         }
+        if (CG == 2) max_groups = d->max_clusters[CG];
     }
-    tgemm_fused_kernel<BN, ST><<<grid, kThreads, L::kDynamicBytes, s>>>(ta, tb, tc, p);
-    return cudaGetLastError();
+    const int groups = static_cast<int>(std::min<int64_t>(tiles, max_groups));
+    if (CG == 1) {
+        kernel<<<groups, kThreads, L::kDynamicBytes, s>>>(ta, tb, tc, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t lc;
+    std::memset(&lc, 0, sizeof(lc));
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeClusterDimension;
+    la[0].val.clusterDim.x = CG;
+    la[0].val.clusterDim.y = 1;
+    la[0].val.clusterDim.z = 1;
+    lc.gridDim = dim3(CG * groups);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = L::kDynamicBytes;
+    lc.stream = s;
+    lc.attrs = la;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kernel, ta, tb, tc, p);
+}
+
+// Fills the tile counts and instruction descriptor for `cfg` and launches.
+cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, const CUtensorMap &tb,
+                          const CUtensorMap &tc, KParams p, cudaStream_t s, bool bf16) {
+    p.num_m = static_cast<int>(cdiv(p.M, kBM * cfg.cg));
+    p.num_n = static_cast<int>(cdiv(p.N, cfg.bn));
+    p.num_kb = static_cast<int>(cdiv(p.K, kBK));
+    const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
+    if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+    p.num_tiles = static_cast<int>(tiles);
+    p.group_m = std::min(p.num_m, 16);
+    p.idesc = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(cfg.bn), false, true);
+    switch (cfg.bit) {
+        case 1: return launch_fused<256, 4, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
+        case 2: return launch_fused<128, 6, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
+        case 4: return launch_fused<64, 8, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
+        case 8: return launch_fused<256, 6, 2>(d, cfg.bit, ta, tb, tc, p, tiles, s);
+        default: return launch_fused<128, 8, 2>(d, cfg.bit, ta, tb, tc, p, tiles, s);
+    }
 }
 
 cudaError_t repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows, int64_t cols,
@@ -285,19 +355,10 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     }
 
     KParams p;
+    std::memset(&p, 0, sizeof(p));
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.num_m = static_cast<int>(cdiv(M, kBM));
-    p.num_n = static_cast<int>(cdiv(N, cfg.bn));
-    p.num_kb = static_cast<int>(cdiv(K, kBK));
-    const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
-    if (tiles > INT32_MAX) {
-        release();
-        return TGEMM_ERR_INVALID_ARG;
-    }
-    p.num_tiles = static_cast<int>(tiles);
-    p.group_m = std::min(p.num_m, 16);
     p.bias = bias;
     p.C = C;
     p.ldc = ldc;
@@ -305,16 +366,8 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     p.relu = relu;
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
-    p.idesc = idesc_f16(bf16, kBM, static_cast<uint32_t>(cfg.bn), false, true);
     p.status = d->status;
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, d->num_sms));
-
-    cudaError_t e;
-    switch (cfg.bn) {
-        case 256: e = launch_fused<256, 4>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
-        case 128: e = launch_fused<128, 6>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
-        default: e = launch_fused<64, 8>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
-    }
+    const cudaError_t e = launch_config(d, cfg, ta, tb, tc, p, stream, bf16);
     release();
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -431,16 +484,10 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
         return TGEMM_ERR_CUDA;
 
     KParams p;
+    std::memset(&p, 0, sizeof(p));
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
-    p.num_m = static_cast<int>(cdiv(M, kBM));
-    p.num_n = static_cast<int>(cdiv(N, cfg.bn));
-    p.num_kb = static_cast<int>(cdiv(K, kBK));
-    const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
-    if (tiles > INT32_MAX) return TGEMM_ERR_INVALID_ARG;
-    p.num_tiles = static_cast<int>(tiles);
-    p.group_m = std::min(p.num_m, 16);
     p.bias = bias;
     p.C = C;
     p.ldc = ldc;
@@ -448,16 +495,8 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
     p.relu = relu;
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
-    p.idesc = idesc_f16(bf16, kBM, static_cast<uint32_t>(cfg.bn), false, true);
     p.status = d->status;
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, d->num_sms));
-
-    cudaError_t e;
-    switch (cfg.bn) {
-        case 256: e = launch_fused<256, 4>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
-        case 128: e = launch_fused<128, 6>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
-        default: e = launch_fused<64, 8>(d, cfg.bit, ta, tb, tc, p, grid, stream); break;
-    }
+    const cudaError_t e = launch_config(d, cfg, ta, tb, tc, p, stream, bf16);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return TGEMM_ERR_CUDA;

@@ -85,13 +85,17 @@ def test_small_and_odd_shapes(cuda_lib, M, N, K):
     assert_close(got, ref, dtype, f"{M}x{N}x{K} {epi} {dtype}", magnitude(inputs, N, K), K)
 
 
-@pytest.mark.parametrize("bn", ["64", "128", "256"])
+CONFIGS = ["64", "128", "256", "128x2", "256x2"]
+
+
+@pytest.mark.parametrize("bn", CONFIGS)
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("epi", ["none", "relu", "bias", "bias_relu"])
 def test_each_tile_config_epilogue_dtype(cuda_lib, monkeypatch, bn, dtype, epi):
     """Several tiles in both directions, a ragged tail on M, N and K, and a k
-    loop longer than the ring (so stages wrap) for each kernel configuration."""
-    monkeypatch.setenv("TGEMM_FORCE_BN", bn)
+    loop longer than the ring (so stages wrap) for each kernel configuration
+    (C tile width, and 1 CTA or a CTA pair per tile)."""
+    monkeypatch.setenv("TGEMM_FORCE_CFG", bn)
     M, N, K = 333, 700, 1000
     inputs, got = run_tgemm(cuda_lib, M, N, K, dtype, epi, seed=5, kind="int")
     assert_bit_exact(got, oracle_ref(inputs, M, N, K, dtype, epi), dtype, f"int bn={bn}")
@@ -100,10 +104,10 @@ def test_each_tile_config_epilogue_dtype(cuda_lib, monkeypatch, bn, dtype, epi):
                  magnitude(inputs, N, K), K)
 
 
-@pytest.mark.parametrize("bn", ["64", "128", "256"])
+@pytest.mark.parametrize("bn", CONFIGS)
 def test_persistent_loop_many_tiles(cuda_lib, monkeypatch, bn):
     """More tiles than SMs: each CTA runs several tiles and both TMEM buffers."""
-    monkeypatch.setenv("TGEMM_FORCE_BN", bn)
+    monkeypatch.setenv("TGEMM_FORCE_CFG", bn)
     M, N, K = 2560, 3072, 192
     inputs, got = run_tgemm(cuda_lib, M, N, K, "bf16", "bias_relu", seed=9, kind="int")
     assert_bit_exact(got, oracle_ref(inputs, M, N, K, "bf16", "bias_relu"), "bf16", f"bn={bn}")
@@ -119,6 +123,15 @@ def test_pitches_and_guarded_padding(cuda_lib, lda, ldb, ldc):
                             lda=lda, ldb=ldb, ldc=ldc)
     assert_pad_untouched(got, N, "pad")
     assert_bit_exact(got[:, :N], oracle_ref(inputs, M, N, K, "fp16", "bias_relu"), "fp16", "pitch")
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_pair_rows_beyond_m(cuda_lib, monkeypatch, cfg):
+    """M that leaves the second CTA of a pair without rows, and tiny M / N."""
+    monkeypatch.setenv("TGEMM_FORCE_CFG", cfg)
+    for (M, N, K) in [(128, 520, 300), (100, 64, 64), (300, 100, 130), (1, 1, 1)]:
+        inputs, got = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=M + N, kind="int")
+        assert_bit_exact(got, oracle_ref(inputs, M, N, K, "fp16", "bias_relu"), "fp16", f"{cfg} {M}x{N}x{K}")
 
 
 # ------------------------------------------------------------------ degenerate
