@@ -57,7 +57,6 @@ constexpr int kBK = 64;           // k per ring stage: 64 x 2 B = one 128-byte s
 constexpr int kUmmaK = 16;        // k per tcgen05.mma (kind::f16)
 constexpr int kThreads = 192;     // 6 warps
 constexpr int kEpiWarps = 4;
-constexpr uint32_t kCStageBytes = 32 * 128;   // 32 rows x 64 columns x 2 B
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kPeerCopyGraceNs = 200000ull;   // 200 us for in-flight copies on abort
 constexpr uint32_t kStatusTimeout = 6;             // TGEMM_ERR_TIMEOUT
@@ -75,10 +74,13 @@ struct KParams {
 
 template <int BN, int STAGES, int CG>
 struct Smem {
-    static constexpr int kBCols = BN / CG;                      // columns of B per CTA
+    static constexpr int kBCols = BN / CG;                      // columns of B per CTA (MMA operand)
+    static constexpr int kBSub = (kBCols + 63) / 64;            // 64-column sub-tiles loaded per CTA
+    static constexpr int kCW = (BN % 64 == 0) ? 64 : 32;        // epilogue chunk width (columns)
     static constexpr uint32_t kABytes = kBM * kBK * 2;          // 16 KiB
-    static constexpr uint32_t kBBytes = kBK * kBCols * 2;       // kBCols/64 sub-tiles of 8 KiB
+    static constexpr uint32_t kBBytes = kBK * 64 * 2 * kBSub;   // kBSub sub-tiles of 8 KiB
     static constexpr uint32_t kStageTx = kABytes + kBBytes;     // bytes one CTA loads per stage
+    static constexpr uint32_t kCStageBytes = 32 * kCW * 2;      // 32 rows x kCW columns
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
     static constexpr uint32_t kOffC = kOffB + STAGES * kBBytes;
@@ -89,11 +91,12 @@ struct Smem {
     static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
     static constexpr uint32_t kBytes = kOffAbort + 4;
     static constexpr uint32_t kDynamicBytes = kBytes + 1024;   // 1 KiB alignment slack
-    static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
-                                          : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    // Accumulator a starts at TMEM column a * kAccStride (a power of two >= BN).
+    static constexpr uint32_t kAccStride = (BN <= 32) ? 32 : (BN <= 64) ? 64 : (BN <= 128) ? 128 : 256;
+    static constexpr uint32_t kTmemCols = (2 * kAccStride < 32) ? 32 : 2 * kAccStride;
     static_assert(CG == 1 || CG == 2, "CTA group of 1 or 2");
-    static_assert(kBCols % 64 == 0, "B is loaded in 64-column sub-tiles");
-    static_assert(2 * BN <= 512, "two accumulators must fit in TMEM");
+    static_assert(BN % 32 == 0 && kBCols % 16 == 0, "tile width");
+    static_assert(kTmemCols <= 512, "two accumulators must fit in TMEM");
     static_assert(kDynamicBytes <= 232448, "shared memory budget exceeded");
     static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "swizzled buffers need 1 KiB alignment");
 };
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(fb, L::kStageTx);
                         tma_load_2d(a_dst, &tmA, fb, kb * kBK, a_row);
 #pragma unroll
-                        for (int j = 0; j < L::kBCols / 64; ++j)
+                        for (int j = 0; j < L::kBSub; ++j)
                             tma_load_2d(b_dst + j * (kBK * 128), &tmB, fb, b_col + j * 64, kb * kBK);
                     } else {
                         // Rank 0 announces the bytes of both CTAs; the peer's copies
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), CG * L::kStageTx);
                         tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, a_row);
 #pragma unroll
-                        for (int j = 0; j < L::kBCols / 64; ++j)
+                        for (int j = 0; j < L::kBSub; ++j)
                             tma_load_2d_pair(b_dst + j * (kBK * 128), &tmB, fb, b_col + j * 64, kb * kBK);
                     }
                     ++uses[stage];
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = group_id; t < p.num_tiles && ok; t += num_groups) {
                 if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * L::kAccStride;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bar(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
@@ -300,13 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        constexpr int CW = L::kCW;               // columns per chunk: 64 (128-byte rows) or 32 (64-byte rows)
+        constexpr int kRowBytes = CW * 2;
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
         const int ew = warp - 2;                 // epilogue warp index 0..3
         int acc = 0;
         uint32_t acc_phase = 0;
         int buf = 0;
-        const uint32_t cstage0 = sbase + L::kOffC + ew * 2 * kCStageBytes;
-        uint8_t *cstage_gen0 = smem + L::kOffC + ew * 2 * kCStageBytes;
+        const uint32_t cstage0 = sbase + L::kOffC + ew * 2 * L::kCStageBytes;
+        uint8_t *cstage_gen0 = smem + L::kOffC + ew * 2 * L::kCStageBytes;
+        // Staging swizzle, matching the C tensor map: 16-byte chunk j of row r
+        // sits at j ^ (r % 8) for 128-byte rows and j ^ ((r / 2) % 4) for 64-byte rows.
+        auto swz = [](int row) { return (CW == 64) ? (row & 7) : ((row >> 1) & 3); };
         auto release_acc = [&](int a) {
             tc_fence_before();
             __syncwarp();
@@ -327,23 +335,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n_tile = n_blk * BN;
             // Only chunks / rows that intersect C are read out and stored (no
             // store is ever issued at a coordinate outside the tensor).
-            const int c_end = (m0 < p.M) ? min(BN / 64, (p.N - n_tile + 63) / 64) : 0;
+            const int c_end = (m0 < p.M) ? min(BN / CW, (p.N - n_tile + CW - 1) / CW) : 0;
             if (c_end == 0) release_acc(acc);
 #pragma unroll 1
             for (int c = 0; c < c_end; ++c) {
-                uint32_t r[64];
+                uint32_t r[CW];
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(acc * BN + c * 64);
-                tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                                       static_cast<uint32_t>(acc) * L::kAccStride + static_cast<uint32_t>(c * CW);
+#pragma unroll
+                for (int h = 0; h < CW / 32; ++h)
+                    tmem_ld_32x32b_x32(taddr + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * h]));
                 tmem_wait_ld();
                 // Last read of this accumulator: hand it back to the MMA lane.
                 if (c == c_end - 1) release_acc(acc);
-                const int n0 = n_tile + c * 64;
-                uint32_t packed[32];
-                const bool full_bias = p.has_bias && (n0 + 64 <= p.N);
+                const int n0 = n_tile + c * CW;
+                uint32_t packed[CW / 2];
+                const bool full_bias = p.has_bias && (n0 + CW <= p.N);
 #pragma unroll
-                for (int g = 0; g < 8; ++g) {
+                for (int g = 0; g < CW / 8; ++g) {
                     float bv[8];
                     if (full_bias) {
                         const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
@@ -380,17 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         packed[g * 4 + h] = pack2(v0, v1, p.is_bf16);
                     }
                 }
-                // Stage the 32 x 64 block: row `lane`, 16-byte chunk j at (j ^ (lane & 7)).
-                const uint32_t sb = cstage0 + buf * kCStageBytes;
-                uint8_t *sb_gen = cstage_gen0 + buf * kCStageBytes;
+                // Stage the 32 x CW block: row `lane`, swizzled 16-byte chunks.
+                const uint32_t sb = cstage0 + buf * L::kCStageBytes;
+                uint8_t *sb_gen = cstage_gen0 + buf * L::kCStageBytes;
                 // A TMA store clips the ragged column edge only at 16-byte
                 // granularity, so a chunk that crosses N takes the masked path.
-                const bool use_tma = p.tma_store && (n0 + 64 <= p.N);
+                const bool use_tma = p.tma_store && (n0 + CW <= p.N);
                 if (p.tma_store && lane == 0) bulk_wait_group_read<1>();   // buffer reused 2 stores later
                 __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t addr = sb + lane * 128 + ((j ^ (lane & 7)) << 4);
+                for (int j = 0; j < CW / 8; ++j) {
+                    const uint32_t addr = sb + lane * kRowBytes + ((j ^ swz(lane)) << 4);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
                                  "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
                                  "r"(packed[4 * j + 3])
@@ -408,16 +417,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Masked, coalesced 2-byte stores: lane l writes columns 2l, 2l+1 of each row.
                     unsigned short *Cg = reinterpret_cast<unsigned short *>(p.C);
                     const int col = n0 + 2 * lane;
+                    if (lane < CW / 2) {
 #pragma unroll 4
-                    for (int rr = 0; rr < 32; ++rr) {
-                        const int row = m0 + rr;
-                        if (row >= p.M) break;
-                        const uint32_t v = *reinterpret_cast<const uint32_t *>(
-                            sb_gen + rr * 128 + ((((lane >> 2) ^ (rr & 7)) << 4) | ((lane & 3) << 2)));
-                        unsigned short *dst = Cg + static_cast<long long>(row) * p.ldc + col;
-                        if (col < p.N) dst[0] = static_cast<unsigned short>(v & 0xFFFFu);
-                        if (col + 1 < p.N) dst[1] = static_cast<unsigned short>(v >> 16);
+                        for (int rr = 0; rr < 32; ++rr) {
+                            const int row = m0 + rr;
+                            if (row >= p.M) break;
+                            const uint32_t v = *reinterpret_cast<const uint32_t *>(
+                                sb_gen + rr * kRowBytes + ((((lane >> 2) ^ swz(rr)) << 4) | ((lane & 3) << 2)));
+                            unsigned short *dst = Cg + static_cast<long long>(row) * p.ldc + col;
+                            if (col < p.N) dst[0] = static_cast<unsigned short>(v & 0xFFFFu);
+                            if (col + 1 < p.N) dst[1] = static_cast<unsigned short>(v >> 16);
+                        }
                     }
+                    __syncwarp();
                 }
                 buf ^= 1;
             }

@@ -159,7 +159,8 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Row-major [rows x cols] 16-bit matrix with pitch `ld`, box [box_rows x box_cols].
+// Row-major [rows x cols] 16-bit matrix with pitch `ld`, box [box_rows x box_cols];
+// the box rows are box_cols * 2 bytes and swizzled at that width (128 or 64 B).
 bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t ld,
               uint32_t box_cols, uint32_t box_rows, bool bf16) {
     EncodeTiledFn enc = encode_fn();
@@ -170,7 +171,8 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int6
     const cuuint32_t estr[2] = {1, 1};
     return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               box_cols * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -181,31 +183,57 @@ struct Cfg {
     int stages;
     int cg;
     int bit;
+    int cw() const { return (bn % 64 == 0) ? 64 : 32; }   // epilogue chunk / C box width
 };
 constexpr Cfg kCfg256 = {256, 4, 1, 1};
+constexpr Cfg kCfg192 = {192, 4, 1, 32};
 constexpr Cfg kCfg128 = {128, 6, 1, 2};
 constexpr Cfg kCfg64 = {64, 8, 1, 4};
 constexpr Cfg kCfg256x2 = {256, 6, 2, 8};
+constexpr Cfg kCfg224x2 = {224, 6, 2, 64};
 constexpr Cfg kCfg128x2 = {128, 8, 2, 16};
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Tile-shape rule.  Per-SM time of a tile is proportional to its width (the
+// MMA rows per SM are fixed at 128), so the estimated kernel time is
+// waves x width x (relative cost per column: narrow single-CTA tiles re-read A
+// from shared memory more often and run slower per column, measured on the
+// 8192^3 workload).  CTA pairs are preferred whenever their tiles fill every
+// SM pair at least once.
 Cfg choose_config(int64_t M, int64_t N, int num_sms) {
     if (const char *f = std::getenv("TGEMM_FORCE_CFG")) {
         const std::string v(f);
         if (v == "256") return kCfg256;
+        if (v == "192") return kCfg192;
         if (v == "128") return kCfg128;
         if (v == "64") return kCfg64;
         if (v == "256x2") return kCfg256x2;
+        if (v == "224x2") return kCfg224x2;
         if (v == "128x2") return kCfg128x2;
     }
-    // A CTA pair (256-row tiles) halves the B operand each SM stages; use it
-    // when the pair tiles still give every SM pair work.
-    if (M > kBM && cdiv(M, 2 * kBM) * cdiv(N, 256) >= num_sms / 2) return kCfg256x2;
-    const int64_t mt = cdiv(M, kBM);
-    if (mt * cdiv(N, 256) >= num_sms) return kCfg256;
-    if (mt * cdiv(N, 128) >= num_sms) return kCfg128;
-    return kCfg64;
+    struct Cand { Cfg cfg; double per_col; };
+    const int pairs = num_sms / 2;
+    if (M > kBM && cdiv(M, 2 * kBM) * cdiv(N, 256) >= pairs) {
+        const Cand cands[2] = {{kCfg256x2, 1.0}, {kCfg224x2, 1.1}};
+        Cfg best = kCfg256x2;
+        double best_cost = 1e300;
+        for (const Cand &c : cands) {
+            const double waves = static_cast<double>(cdiv(cdiv(M, 2 * kBM) * cdiv(N, c.cfg.bn), pairs));
+            const double cost = waves * c.cfg.bn * c.per_col;
+            if (cost < best_cost) { best_cost = cost; best = c.cfg; }
+        }
+        return best;
+    }
+    const Cand cands[4] = {{kCfg256, 1.0}, {kCfg192, 1.2}, {kCfg128, 1.5}, {kCfg64, 3.0}};
+    Cfg best = kCfg256;
+    double best_cost = 1e300;
+    for (const Cand &c : cands) {
+        const double waves = static_cast<double>(cdiv(cdiv(M, kBM) * cdiv(N, c.cfg.bn), num_sms));
+        const double cost = waves * c.cfg.bn * c.per_col;
+        if (cost < best_cost) { best_cost = cost; best = c.cfg; }
+    }
+    return best;
 }
 
 template <int BN, int ST, int CG>
@@ -281,7 +309,9 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
         case 2: return launch_fused<128, 6, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
         case 4: return launch_fused<64, 8, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
         case 8: return launch_fused<256, 6, 2>(d, cfg.bit, ta, tb, tc, p, tiles, s);
-        default: return launch_fused<128, 8, 2>(d, cfg.bit, ta, tb, tc, p, tiles, s);
+        case 16: return launch_fused<128, 8, 2>(d, cfg.bit, ta, tb, tc, p, tiles, s);
+        case 32: return launch_fused<192, 4, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
+        default: return launch_fused<224, 6, 2>(d, cfg.bit, ta, tb, tc, p, tiles, s);
     }
 }
 
@@ -349,7 +379,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     std::memset(&tc, 0, sizeof(tc));
     if (!make_map(&ta, a_use, M, K, lda_use, kBK, kBM, bf16) ||
         !make_map(&tb, b_use, K, N, ldb_use, 64, kBK, bf16) ||
-        (tma_store && !make_map(&tc, C, M, N, ldc, 64, 32, bf16))) {
+        (tma_store && !make_map(&tc, C, M, N, ldc, cfg.cw(), 32, bf16))) {
         release();
         return TGEMM_ERR_CUDA;
     }
@@ -480,7 +510,7 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
     std::memset(&tc, 0, sizeof(tc));
     if (!make_map(&ta, a_use, M, K, lda_use, kBK, kBM, bf16) ||
         !make_map(&tb, b_use, K, N, ldb_use, 64, kBK, bf16) ||
-        (tma_store && !make_map(&tc, C, M, N, ldc, 64, 32, bf16)))
+        (tma_store && !make_map(&tc, C, M, N, ldc, cfg.cw(), 32, bf16)))
         return TGEMM_ERR_CUDA;
 
     KParams p;

@@ -85,7 +85,7 @@ def test_small_and_odd_shapes(cuda_lib, M, N, K):
     assert_close(got, ref, dtype, f"{M}x{N}x{K} {epi} {dtype}", magnitude(inputs, N, K), K)
 
 
-CONFIGS = ["64", "128", "256", "128x2", "256x2"]
+CONFIGS = ["64", "128", "192", "256", "128x2", "224x2", "256x2"]
 
 
 @pytest.mark.parametrize("bn", CONFIGS)
