@@ -304,6 +304,10 @@ def run_tgemm_bench(args, world, rank, local):
         barrier(world)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     mean_ms = sum(launch_ms) / len(launch_ms)
+    srt = sorted(launch_ms)
+    pct = lambda f: srt[min(len(srt) - 1, int(f * len(srt)))] * 1e3
+    launch_stats = {"mean": mean_ms * 1e3, "p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9),
+                    "max": srt[-1] * 1e3, "wall_per_step": t_wall / args.steps * 1e6}
     mean_ms_max = max_over_ranks(mean_ms, world)
     value = world * flops / (mean_ms_max * 1e-3) / 1e12
 
@@ -352,6 +356,7 @@ def run_tgemm_bench(args, world, rank, local):
                          "algorithmic_bytes_per_launch": (w.M * w.K + w.K * w.N + w.M * w.N + w.N) * 2},
             "clocks": clk.summary(),
             "gpu_launches": args.steps * (1 + (1 if (w.lda or w.K) % 8 else 0) + (1 if (w.ldb or w.N) % 8 else 0)),
+            "launch_us": launch_stats,
             "device_status": tg.tgemm_status_string(status),
             "wall_s_timed_region": t_wall}
     if e2e is not None:

@@ -7,17 +7,37 @@
 namespace tgemm {
 
 // Copy a [rows x cols] 16-bit matrix from pitch `lds` to pitch `ldd` (ldd a
-// multiple of 8 elements), so that tensor-memory-access copies, which need
-// 16-byte row strides, can read an operand whose own pitch is unaligned.
-__global__ void repack_rows_kernel(const uint16_t *__restrict__ src, long long lds,
-                                   uint16_t *__restrict__ dst, long long ldd, long long rows,
-                                   long long cols) {
+// multiple of 8 elements, dst 16-byte aligned), so that tensor-memory-access
+// copies, which need 16-byte row strides, can read an operand whose own pitch
+// is unaligned.  Each thread writes one 16-byte vector of a destination row
+// (8 elements) from 8 coalesced 2-byte source reads; blockIdx.y walks rows.
+// HBM-bound: 2 x rows x cols x 2 bytes.
+__global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t *__restrict__ src, long long lds,
+                                                          uint16_t *__restrict__ dst, long long ldd,
+                                                          long long rows, long long cols) {
+    const long long vec_per_row = (cols + 7) / 8;
     for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
         const uint16_t *s = src + r * lds;
-        uint16_t *d = dst + r * ldd;
-        for (long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; c < cols;
-             c += static_cast<long long>(gridDim.x) * blockDim.x)
-            d[c] = s[c];
+        uint4 *d = reinterpret_cast<uint4 *>(dst + r * ldd);
+        for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < vec_per_row;
+             v += static_cast<long long>(gridDim.x) * blockDim.x) {
+            const long long c0 = v * 8;
+            uint32_t w[4];
+            if (c0 + 8 <= cols) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    w[i] = static_cast<uint32_t>(__ldg(s + c0 + 2 * i)) |
+                           (static_cast<uint32_t>(__ldg(s + c0 + 2 * i + 1)) << 16);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t lo = (c0 + 2 * i < cols) ? __ldg(s + c0 + 2 * i) : 0u;
+                    const uint32_t hi = (c0 + 2 * i + 1 < cols) ? __ldg(s + c0 + 2 * i + 1) : 0u;
+                    w[i] = lo | (hi << 16);
+                }
+            }
+            d[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     }
 }
 

@@ -302,7 +302,9 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
     if (tiles > INT32_MAX) return cudaErrorInvalidValue;
     p.num_tiles = static_cast<int>(tiles);
-    p.group_m = std::min(p.num_m, 16);
+    int group_m = 16;
+    if (const char *g = std::getenv("TGEMM_GROUP_M")) group_m = std::max(1, std::atoi(g));
+    p.group_m = std::min(p.num_m, group_m);
     p.idesc = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(cfg.bn), false, true);
     switch (cfg.bit) {
         case 1: return launch_fused<256, 4, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
@@ -318,7 +320,7 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
 cudaError_t repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows, int64_t cols,
                    cudaStream_t s) {
     const dim3 block(256);
-    const dim3 grid(static_cast<unsigned>(std::min<int64_t>(cdiv(cols, 256), 64)),
+    const dim3 grid(static_cast<unsigned>(std::min<int64_t>(cdiv(cdiv(cols, 8), 256), 64)),
                     static_cast<unsigned>(std::min<int64_t>(rows, 65535)));
     repack_rows_kernel<<<grid, block, 0, s>>>(static_cast<const uint16_t *>(src), lds,
                                               static_cast<uint16_t *>(dst), ldd, rows, cols);
