@@ -35,6 +35,8 @@ struct DeviceInfo {
     std::mutex mu;          // guards lazily set kernel attributes
     unsigned attr_set = 0;  // bit per kernel configuration
     int max_clusters[3] = {0, 0, 0};   // co-resident clusters per CTA-group size
+    cudaStream_t copy_in = nullptr;    // tgemm_run_host: host->device copies
+    cudaStream_t copy_out = nullptr;   // tgemm_run_host: device->host copies
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -583,6 +585,13 @@ extern "C" tgemm_status tgemm_run(const void *A, const void *B, const void *bias
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
+// End-to-end call on host buffers.  The device copies use compact 16-byte
+// pitches (the 2-D copies do any repacking), and the work is pipelined over
+// chunks of rows of A / C: chunk i's host->device copy, chunk i-1's GEMM and
+// chunk i-2's device->host copy run concurrently on three streams (copies in,
+// the caller's stream for the GEMMs, copies out).  When B carries most of the
+// host traffic the problem runs as one chunk: column chunks of a row-major B
+// are narrow strided copies that move far slower than one contiguous copy.
 extern "C" tgemm_status tgemm_run_host(const void *A_host, const void *B_host,
                                        const void *bias_host, void *C_host, int64_t M, int64_t N,
                                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
@@ -595,39 +604,125 @@ extern "C" tgemm_status tgemm_run_host(const void *A_host, const void *B_host,
     st = current_device(&d);
     if (st != TGEMM_OK) return st;
     if (M == 0 || N == 0) return TGEMM_OK;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    cudaStream_t s0 = reinterpret_cast<cudaStream_t>(stream_);
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    {
+        std::lock_guard<std::mutex> g(d->mu);
+        if (!d->copy_in && (cudaStreamCreateWithFlags(&d->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
+                            cudaStreamCreateWithFlags(&d->copy_out, cudaStreamNonBlocking) != cudaSuccess)) {
+            cudaGetLastError();
+            return TGEMM_ERR_CUDA;
+        }
+        s_in = d->copy_in;
+        s_out = d->copy_out;
+    }
     const bool use_bias = epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU;
-    void *dA = nullptr, *dB = nullptr, *dbias = nullptr, *dC = nullptr;
+    const int64_t lda_d = cdiv(K, 8) * 8, ldb_d = cdiv(N, 8) * 8, ldc_d = cdiv(N, 8) * 8;
+    unsigned char *dA = nullptr, *dB = nullptr, *dbias = nullptr, *dC = nullptr;
     bool ok = true;
-    auto alloc = [&](void **p, size_t bytes) {
-        if (ok && cudaMallocFromPoolAsync(p, bytes, d->pool, stream) != cudaSuccess) ok = false;
+    auto check = [&](cudaError_t e) { if (e != cudaSuccess) ok = false; return ok; };
+    auto alloc = [&](unsigned char **p, int64_t bytes) {
+        if (ok) check(cudaMallocFromPoolAsync(reinterpret_cast<void **>(p), static_cast<size_t>(bytes), d->pool, s0));
     };
     if (K > 0) {
-        alloc(&dA, static_cast<size_t>(M * lda * 2));
-        alloc(&dB, static_cast<size_t>(K * ldb * 2));
+        alloc(&dA, M * lda_d * 2);
+        alloc(&dB, K * ldb_d * 2);
     }
-    if (use_bias) alloc(&dbias, static_cast<size_t>(N * 2));
-    alloc(&dC, static_cast<size_t>(M * ldc * 2));
-    if (ok && K > 0) {
-        ok = cudaMemcpy2DAsync(dA, lda * 2, A_host, lda * 2, K * 2, M, cudaMemcpyHostToDevice,
-                               stream) == cudaSuccess &&
-             cudaMemcpy2DAsync(dB, ldb * 2, B_host, ldb * 2, N * 2, K, cudaMemcpyHostToDevice,
-                               stream) == cudaSuccess;
+    if (use_bias) alloc(&dbias, cdiv(N, 8) * 16);
+    alloc(&dC, M * ldc_d * 2);
+
+    // Chunking: along M when A and C carry most of the host traffic (about
+    // 16 MiB of host traffic per chunk, at most 8 chunks), else one chunk.
+    const bool by_rows = M * (K + N) >= K * N;
+    const int64_t host_bytes = (M * K + K * N + M * N) * 2;
+    const int64_t want =
+        by_rows ? std::max<int64_t>(1, std::min<int64_t>(8, host_bytes / (16ll << 20))) : 1;
+    const int64_t extent = by_rows ? M : N;
+    const int64_t step = std::max<int64_t>(256, cdiv(cdiv(extent, want), 256) * 256);
+    const int64_t nch = cdiv(extent, step);
+
+    cudaEvent_t e_ready = nullptr, e_in_fixed = nullptr, e_done = nullptr;
+    cudaEvent_t e_in[8] = {}, e_gemm[8] = {};
+    auto mk = [&](cudaEvent_t *e) { if (ok) check(cudaEventCreateWithFlags(e, cudaEventDisableTiming)); };
+    mk(&e_ready);
+    mk(&e_in_fixed);
+    mk(&e_done);
+    for (int64_t i = 0; i < nch; ++i) {
+        mk(&e_in[i]);
+        mk(&e_gemm[i]);
     }
-    if (ok && use_bias)
-        ok = cudaMemcpyAsync(dbias, bias_host, N * 2, cudaMemcpyHostToDevice, stream) == cudaSuccess;
-    if (ok) {
-        st = run_device(d, dA, dB, dbias, dC, M, N, K, lda, ldb, ldc, dtype, epilogue, stream);
-        if (st == TGEMM_OK &&
-            cudaMemcpy2DAsync(C_host, ldc * 2, dC, ldc * 2, N * 2, M, cudaMemcpyDeviceToHost,
-                              stream) != cudaSuccess)
-            st = TGEMM_ERR_CUDA;
-    } else {
-        st = TGEMM_ERR_CUDA;
+    const char *Ah = static_cast<const char *>(A_host);
+    const char *Bh = static_cast<const char *>(B_host);
+    char *Ch = static_cast<char *>(C_host);
+
+    if (ok) check(cudaEventRecord(e_ready, s0));
+    if (ok) check(cudaStreamWaitEvent(s_in, e_ready, 0));
+    // Operands every chunk needs: B (row chunks) or A (column chunks), and the bias.
+    if (ok && K > 0 && by_rows)
+        check(cudaMemcpy2DAsync(dB, ldb_d * 2, Bh, ldb * 2, N * 2, K, cudaMemcpyHostToDevice, s_in));
+    if (ok && K > 0 && !by_rows)
+        check(cudaMemcpy2DAsync(dA, lda_d * 2, Ah, lda * 2, K * 2, M, cudaMemcpyHostToDevice, s_in));
+    if (ok && use_bias) check(cudaMemcpyAsync(dbias, bias_host, N * 2, cudaMemcpyHostToDevice, s_in));
+    if (ok) check(cudaEventRecord(e_in_fixed, s_in));
+    for (int64_t i = 0; i < nch && ok; ++i) {
+        const int64_t lo = i * step, hi = std::min(extent, lo + step);
+        if (K > 0 && by_rows)
+            check(cudaMemcpy2DAsync(dA + lo * lda_d * 2, lda_d * 2, Ah + lo * lda * 2, lda * 2, K * 2, hi - lo,
+                                    cudaMemcpyHostToDevice, s_in));
+        if (ok && K > 0 && !by_rows)
+            check(cudaMemcpy2DAsync(dB + lo * 2, ldb_d * 2, Bh + lo * 2, ldb * 2, (hi - lo) * 2, K,
+                                    cudaMemcpyHostToDevice, s_in));
+        if (ok) check(cudaEventRecord(e_in[i], s_in));
     }
-    for (void *p : {dA, dB, dbias, dC})
-        if (p) cudaFreeAsync(p, stream);
-    if (st != TGEMM_OK) cudaGetLastError();
+    if (ok) check(cudaStreamWaitEvent(s0, e_in_fixed, 0));
+    for (int64_t i = 0; i < nch && ok; ++i) {
+        const int64_t lo = i * step, hi = std::min(extent, lo + step);
+        check(cudaStreamWaitEvent(s0, e_in[i], 0));
+        if (!ok) break;
+        tgemm_status g;
+        if (by_rows)
+            g = run_device(d, K > 0 ? dA + lo * lda_d * 2 : nullptr, dB, dbias, dC + lo * ldc_d * 2, hi - lo, N, K,
+                           lda_d, ldb_d, ldc_d, dtype, epilogue, s0);
+        else
+            g = run_device(d, dA, K > 0 ? dB + lo * 2 : nullptr, use_bias ? dbias + lo * 2 : nullptr, dC + lo * 2,
+                           M, hi - lo, K, lda_d, ldb_d, ldc_d, dtype, epilogue, s0);
+        if (g != TGEMM_OK) {
+            st = g;
+            ok = false;
+            break;
+        }
+        check(cudaEventRecord(e_gemm[i], s0));
+    }
+    for (int64_t i = 0; i < nch && ok; ++i) {
+        const int64_t lo = i * step, hi = std::min(extent, lo + step);
+        check(cudaStreamWaitEvent(s_out, e_gemm[i], 0));
+        if (ok && by_rows)
+            check(cudaMemcpy2DAsync(Ch + lo * ldc * 2, ldc * 2, dC + lo * ldc_d * 2, ldc_d * 2, N * 2, hi - lo,
+                                    cudaMemcpyDeviceToHost, s_out));
+        if (ok && !by_rows)
+            check(cudaMemcpy2DAsync(Ch + lo * 2, ldc * 2, dC + lo * 2, ldc_d * 2, (hi - lo) * 2, M,
+                                    cudaMemcpyDeviceToHost, s_out));
+    }
+    // Join both copy streams back into the caller's stream before the buffers
+    // return to the pool, whatever happened above.
+    if (e_done) {
+        cudaEventRecord(e_done, s_out);
+        cudaStreamWaitEvent(s0, e_done, 0);
+        cudaEventRecord(e_done, s_in);
+        cudaStreamWaitEvent(s0, e_done, 0);
+    }
+    for (unsigned char *p : {dA, dB, dbias, dC})
+        if (p) cudaFreeAsync(p, s0);
+    for (cudaEvent_t e : {e_ready, e_in_fixed, e_done})
+        if (e) cudaEventDestroy(e);
+    for (int64_t i = 0; i < nch; ++i) {
+        if (e_in[i]) cudaEventDestroy(e_in[i]);
+        if (e_gemm[i]) cudaEventDestroy(e_gemm[i]);
+    }
+    if (!ok) {
+        cudaGetLastError();
+        if (st == TGEMM_OK) st = TGEMM_ERR_CUDA;
+    }
     return st;
 }
 

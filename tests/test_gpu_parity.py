@@ -186,6 +186,30 @@ def test_host_entry_point_matches_device_entry_point(cuda_lib):
     assert np.isnan(Ch[:, N:].float().numpy()).all()
 
 
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc", [
+    (4096, 4096, 1024, 1027, 4096, 4100),     # chunks of rows of A / C, unaligned host pitches
+    (128, 16384, 8192, 8192, 16389, 16384),   # B dominates: one chunk, unaligned B pitch
+])
+def test_host_entry_point_pipelined_chunks(cuda_lib, M, N, K, lda, ldb, ldc):
+    """The host path splits large problems into chunks whose copies and GEMMs
+    overlap on separate streams; results equal the device entry point's."""
+    A, B, bias = si.make_inputs(M, N, K, "fp16", seed=23, lda=lda if lda != K else None,
+                                ldb=ldb if ldb != N else None)
+    dev = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    cuda_lib.run(A.cuda()[:, :K], B.cuda()[:, :N], bias.cuda(), dev, "bias_relu")
+    Ah, Bh, bh = A.pin_memory(), B.pin_memory(), bias.pin_memory()
+    Ch = torch.full((M, ldc), float("nan"), dtype=torch.float16).pin_memory()
+    cuda_lib.run_host(Ah[:, :K], Bh[:, :N], bh, Ch[:, :N], "bias_relu")
+    torch.cuda.synchronize()
+    got = Ch.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got[:, :N], dev.cpu().view(torch.int16).numpy().view(np.uint16))
+    if ldc > N:
+        assert np.isnan(Ch[:, N:].float().numpy()).all()
+    rows = sample_rows(M, n=8, seed=5)
+    ref = oracle_ref((A, B, bias), M, N, K, "fp16", "bias_relu", rows=rows)
+    assert_close(got[rows, :N], ref, "fp16", "host path", magnitude((A, B, bias), N, K, rows), K)
+
+
 def test_host_memory_passed_to_device_entry_point_is_rejected(cuda_lib):
     A = torch.ones((64, 64), dtype=torch.float16)
     Cd = torch.empty((64, 64), dtype=torch.float16, device="cuda")
