@@ -37,6 +37,11 @@ import torch  # noqa: E402
 import seeded_inputs as si  # noqa: E402
 
 METRIC = "fused GEMM+bias+ReLU TFLOP/s (2MNK/t) on 1 GB300; % of dense fp16 tensor peak"
+METRIC_GELU = "fused GEMM+bias+GELU TFLOP/s (2MNK/t) on 1 GB300; % of dense fp16 tensor peak"
+
+
+def metric_for(w):
+    return METRIC_GELU if "gelu" in w.epilogue else METRIC
 DEFAULT_WORKLOAD = "c1"
 FLUSH_BYTES = 256 << 20            # > 2x the 129 MB L2
 KERNEL_SOURCES = ["gemm_epilogue_02_gb300/csrc/gemm_kernel.cuh", "gemm_epilogue_02_gb300/csrc/ptx.cuh",
@@ -235,7 +240,7 @@ def run_reference(args, world, rank):
     t = sum(times) / len(times)
     value = 2.0 * len(rows) * w.N * w.K / t / 1e12
     sample = f"first {len(rows)} of {w.M} rows of {w.name} per step (all {w.N} columns, K={w.K}), fp64"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+    line = {"impl": "reference", "metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(w),
@@ -345,7 +350,7 @@ def run_tgemm_bench(args, world, rank, local):
     peak, hbm, peak_kind = measured_peaks()
     achieved = flops / (mean_ms * 1e-3) / 1e12
     traffic = recorded_traffic(args.config)
-    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+    line = {"metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup_done, "ms_per_step": mean_ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic", "config": workload_config(w),

@@ -9,7 +9,8 @@ from __future__ import annotations
 import torch
 
 from ._binding import (  # noqa: F401
-    TGEMM_BF16, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_RELU, TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_F16,
+    TGEMM_BF16, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_GELU, TGEMM_EPI_BIAS_RELU, TGEMM_EPI_GELU,
+    TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_F16,
     EXPORTED, NOALLOC_SCRATCH_BYTES, STATUS, TgemmError, library_path, load,
     tgemm_last_device_status, tgemm_run, tgemm_run_host, tgemm_run_noalloc, tgemm_status_string,
     tgemm_version,
@@ -17,7 +18,7 @@ from ._binding import (  # noqa: F401
 from .build import build  # noqa: F401
 
 EPILOGUES = {"none": TGEMM_EPI_NONE, "relu": TGEMM_EPI_RELU, "bias": TGEMM_EPI_BIAS,
-             "bias_relu": TGEMM_EPI_BIAS_RELU}
+             "bias_relu": TGEMM_EPI_BIAS_RELU, "gelu": TGEMM_EPI_GELU, "bias_gelu": TGEMM_EPI_BIAS_GELU}
 _DT = {torch.float16: TGEMM_F16, torch.bfloat16: TGEMM_BF16}
 
 

@@ -14,6 +14,7 @@ from . import build as _build
 
 TGEMM_F16, TGEMM_BF16 = 0, 1
 TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_RELU = 0, 1, 2, 3
+TGEMM_EPI_GELU, TGEMM_EPI_BIAS_GELU = 4, 5
 STATUS = {0: "TGEMM_OK", 1: "TGEMM_ERR_INVALID_ARG", 2: "TGEMM_ERR_ALIGNMENT",
           3: "TGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TGEMM_ERR_ALIAS", 5: "TGEMM_ERR_CUDA",
           6: "TGEMM_ERR_TIMEOUT", 7: "TGEMM_ERR_SCRATCH_LIMIT"}

@@ -42,8 +42,9 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t *__rest
 }
 
 // K == 0: the empty sum is 0, so C[i, j] = epi(bias[j]) (or epi(0)).
+// act: 0 none, 1 ReLU, 2 GELU (the same activations as the fused kernel).
 __global__ void fill_epilogue_kernel(const uint16_t *__restrict__ bias, uint16_t *__restrict__ C,
-                                     long long ldc, int M, int N, int has_bias, int relu,
+                                     long long ldc, int M, int N, int has_bias, int act,
                                      int is_bf16) {
     for (long long r = blockIdx.y; r < M; r += gridDim.y) {
         for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < N; j += gridDim.x * blockDim.x) {
@@ -51,7 +52,11 @@ __global__ void fill_epilogue_kernel(const uint16_t *__restrict__ bias, uint16_t
             if (has_bias)
                 v = is_bf16 ? __bfloat162float(__ushort_as_bfloat16(bias[j]))
                             : __half2float(__ushort_as_half(bias[j]));
-            if (relu) v = (v <= 0.0f) ? 0.0f : v;
+            if (act == 1) v = (v <= 0.0f) ? 0.0f : v;
+            if (act == 2) {
+                const float u = 1.5957691216f * fmaf(0.044715f * v, v * v, v);
+                v = v * __frcp_rn(1.0f + __expf(-u));
+            }
             const uint16_t out = is_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
                                          : __half_as_ushort(__float2half_rn(v));
             C[r * ldc + j] = out;

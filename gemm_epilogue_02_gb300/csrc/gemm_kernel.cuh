@@ -27,8 +27,10 @@
 //               lane issues tcgen05.mma (M = 128*CG, N = BN, K = 16) per 16-wide
 //               k step; a tcgen05.commit frees each ring stage (in both CTAs)
 //               and publishes each finished accumulator (to both CTAs).
-//   warps 2..5  epilogue: tcgen05.ld TMEM -> registers (each warp owns the 32
-//               TMEM lanes = 32 rows its warp index allows), + bias, ReLU,
+//   warps 2..9  epilogue: tcgen05.ld TMEM -> registers (each warp owns the 32
+//               TMEM lanes = 32 rows its warp index allows; two warps share a
+//               lane quarter and take alternate column chunks, the next chunk's
+//               load in flight while one is processed), + bias, ReLU or GELU,
 //               round to fp16/bf16, 128B-swizzled staging in shared memory,
 //               then a TMA store (clipped at the ragged M edge) or masked
 //               coalesced stores (a chunk crossing the ragged N edge, or a C
@@ -48,6 +50,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace tgemm {
@@ -55,8 +59,8 @@ namespace tgemm {
 constexpr int kBM = 128;          // rows per CTA (TMEM lanes)
 constexpr int kBK = 64;           // k per ring stage: 64 x 2 B = one 128-byte swizzle row
 constexpr int kUmmaK = 16;        // k per tcgen05.mma (kind::f16)
-constexpr int kThreads = 192;     // 6 warps
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, alternating chunks
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer, MMA, epilogue warps
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kPeerCopyGraceNs = 200000ull;   // 200 us for in-flight copies on abort
 constexpr uint32_t kStatusTimeout = 6;             // TGEMM_ERR_TIMEOUT
@@ -67,7 +71,7 @@ struct KParams {
     const void *bias;          // may be null when !has_bias
     void *C;                   // used by the masked-store path only
     long long ldc;
-    int has_bias, relu, is_bf16, tma_store;
+    int has_bias, act, is_bf16, tma_store;   // act: 0 none, 1 ReLU, 2 GELU
     uint32_t idesc;
     unsigned int *status;      // device status word
 };
@@ -84,7 +88,10 @@ struct Smem {
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
     static constexpr uint32_t kOffC = kOffB + STAGES * kBBytes;
-    static constexpr uint32_t kOffBar = kOffC + kEpiWarps * 2 * kCStageBytes;
+    // Staging buffers per epilogue warp: two when they fit, else one.
+    static constexpr uint32_t kCBufs =
+        (kOffC + kEpiWarps * 2 * kCStageBytes + 2048 <= 232448) ? 2 : 1;
+    static constexpr uint32_t kOffBar = kOffC + kEpiWarps * kCBufs * kCStageBytes;
     // full[S], empty[S], tfull[2], tempty[2], drain
     static constexpr uint32_t kNumBars = 2 * STAGES + 5;
     static constexpr uint32_t kOffTmemHolder = kOffBar + kNumBars * 8;
@@ -145,6 +152,20 @@ __device__ __forceinline__ float bias_val(const void *bias, int idx, int is_bf16
 __device__ __forceinline__ float epi_relu(float v) {
     // x <= 0 (incl. -0.0) -> +0.0; NaN compares false and is kept.
     return (v <= 0.0f) ? 0.0f : v;
+}
+
+// The tanh-form GELU of "TileLang で GPU カーネル設計を解説" §4, written as a
+// sigmoid: x / (1 + exp(-1.5957691216 (x + 0.044715 x^3))).  Large negative x
+// gives exp -> inf and x * 0 = -0; NaN propagates.
+__device__ __forceinline__ float epi_gelu(float x) {
+    const float u = 1.5957691216f * fmaf(0.044715f * x, x * x, x);
+    return __fdividef(x, 1.0f + __expf(-u));
+}
+
+__device__ __forceinline__ float epi_act(float v, int act) {
+    if (act == 1) return epi_relu(v);
+    if (act == 2) return epi_gelu(v);
+    return v;
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
@@ -305,13 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         constexpr int CW = L::kCW;               // columns per chunk: 64 (128-byte rows) or 32 (64-byte rows)
         constexpr int kRowBytes = CW * 2;
+        const int ew = warp - 2;                 // epilogue warp index 0..kEpiWarps-1
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
-        const int ew = warp - 2;                 // epilogue warp index 0..3
+        const int part = ew >> 2;                // chunks part, part + 2, ... of each tile
         int acc = 0;
         uint32_t acc_phase = 0;
         int buf = 0;
-        const uint32_t cstage0 = sbase + L::kOffC + ew * 2 * L::kCStageBytes;
-        uint8_t *cstage_gen0 = smem + L::kOffC + ew * 2 * L::kCStageBytes;
+        const uint32_t cstage0 = sbase + L::kOffC + ew * L::kCBufs * L::kCStageBytes;
+        uint8_t *cstage_gen0 = smem + L::kOffC + ew * L::kCBufs * L::kCStageBytes;
         // Staging swizzle, matching the C tensor map: 16-byte chunk j of row r
         // sits at j ^ (r % 8) for 128-byte rows and j ^ ((r / 2) % 4) for 64-byte rows.
         auto swz = [](int row) { return (CW == 64) ? (row & 7) : ((row >> 1) & 3); };
@@ -336,27 +358,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Only chunks / rows that intersect C are read out and stored (no
             // store is ever issued at a coordinate outside the tensor).
             const int c_end = (m0 < p.M) ? min(BN / CW, (p.N - n_tile + CW - 1) / CW) : 0;
-            if (c_end == 0) release_acc(acc);
-#pragma unroll 1
-            for (int c = 0; c < c_end; ++c) {
-                uint32_t r[CW];
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(acc) * L::kAccStride + static_cast<uint32_t>(c * CW);
-#pragma unroll
-                for (int h = 0; h < CW / 32; ++h)
-                    tmem_ld_32x32b_x32(taddr + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * h]));
-                tmem_wait_ld();
-                // Last read of this accumulator: hand it back to the MMA lane.
-                if (c == c_end - 1) release_acc(acc);
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc) * L::kAccStride;
+            // TMEM is read in 32-column sub-chunks; a chunk is CW / 32 of them.
+            constexpr int SUBS = CW / 32;
+            const int my_chunks = (c_end > part) ? (c_end - part + 1) / 2 : 0;
+            const int n_sub = my_chunks * SUBS;
+            auto chunk_of = [&](int sub) { return part + 2 * (sub / SUBS); };
+            auto tload = [&](int sub, uint32_t (&r)[32]) {
+                tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(chunk_of(sub) * CW + 32 * (sub % SUBS)), r);
+            };
+            uint32_t packed[CW / 2];
+            // + bias and activation for sub-chunk H of a chunk, one rounding into
+            // `packed`; after the last sub-chunk, swizzled staging and the store.
+            auto process = [&](auto hc, int sub, const uint32_t (&r)[32]) {
+                constexpr int H = decltype(hc)::value;
+                const int c = chunk_of(sub);
                 const int n0 = n_tile + c * CW;
-                uint32_t packed[CW / 2];
-                const bool full_bias = p.has_bias && (n0 + CW <= p.N);
+                const int nh = n0 + 32 * H;
+                const bool full_bias = p.has_bias && (nh + 32 <= p.N);
 #pragma unroll
-                for (int g = 0; g < CW / 8; ++g) {
+                for (int g = 0; g < 4; ++g) {
                     float bv[8];
                     if (full_bias) {
                         const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-                                                    reinterpret_cast<const unsigned short *>(p.bias) + n0) +
+                                                    reinterpret_cast<const unsigned short *>(p.bias) + nh) +
                                                 g);
                         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -374,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else if (p.has_bias) {
 #pragma unroll
                         for (int h = 0; h < 8; ++h) {
-                            const int col = n0 + g * 8 + h;
+                            const int col = nh + g * 8 + h;
                             bv[h] = (col < p.N) ? bias_val(p.bias, col, p.is_bf16) : 0.0f;
                         }
                     } else {
@@ -385,17 +411,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < 4; ++h) {
                         float v0 = __uint_as_float(r[g * 8 + 2 * h]) + bv[2 * h];
                         float v1 = __uint_as_float(r[g * 8 + 2 * h + 1]) + bv[2 * h + 1];
-                        if (p.relu) { v0 = epi_relu(v0); v1 = epi_relu(v1); }
-                        packed[g * 4 + h] = pack2(v0, v1, p.is_bf16);
+                        v0 = epi_act(v0, p.act);
+                        v1 = epi_act(v1, p.act);
+                        packed[16 * H + g * 4 + h] = pack2(v0, v1, p.is_bf16);
                     }
                 }
+                if constexpr (H != SUBS - 1) return;
                 // Stage the 32 x CW block: row `lane`, swizzled 16-byte chunks.
                 const uint32_t sb = cstage0 + buf * L::kCStageBytes;
                 uint8_t *sb_gen = cstage_gen0 + buf * L::kCStageBytes;
                 // A TMA store clips the ragged column edge only at 16-byte
                 // granularity, so a chunk that crosses N takes the masked path.
                 const bool use_tma = p.tma_store && (n0 + CW <= p.N);
-                if (p.tma_store && lane == 0) bulk_wait_group_read<1>();   // buffer reused 2 stores later
+                if (p.tma_store && lane == 0) {
+                    if constexpr (L::kCBufs == 2) bulk_wait_group_read<1>();   // buffer reused 2 stores later
+                    else bulk_wait_group_read<0>();
+                }
                 __syncwarp();
 #pragma unroll
                 for (int j = 0; j < CW / 8; ++j) {
@@ -431,7 +462,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                 }
-                buf ^= 1;
+                if constexpr (L::kCBufs == 2) buf ^= 1;
+            };
+            if (n_sub == 0) {
+                release_acc(acc);
+            } else {
+                // The next sub-chunk's TMEM load is in flight while one is processed;
+                // the accumulator goes back to the MMA lane as soon as its last load
+                // lands.  Sub-chunks alternate between ra (even: first half of a chunk)
+                // and rb (odd: second half when a chunk has two).
+                uint32_t ra[32], rb[32];
+                int sub = 0;
+                tload(sub, ra);
+                tmem_wait_ld();
+#pragma unroll 1
+                for (;;) {
+                    bool more = sub + 1 < n_sub;
+                    if (more) tload(sub + 1, rb);
+                    else release_acc(acc);
+                    process(std::integral_constant<int, 0>{}, sub, ra);
+                    if (!more) break;
+                    tmem_wait_ld();
+                    ++sub;
+                    more = sub + 1 < n_sub;
+                    if (more) tload(sub + 1, ra);
+                    else release_acc(acc);
+                    process(std::integral_constant<int, SUBS - 1>{}, sub, rb);
+                    if (!more) break;
+                    tmem_wait_ld();
+                    ++sub;
+                }
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }

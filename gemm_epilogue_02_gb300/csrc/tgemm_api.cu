@@ -104,6 +104,17 @@ bool overlaps(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool uses_bias(int epi) {
+    return epi == TGEMM_EPI_BIAS || epi == TGEMM_EPI_BIAS_RELU || epi == TGEMM_EPI_BIAS_GELU;
+}
+
+// Activation code of the kernels: 0 none, 1 ReLU, 2 GELU.
+int activation(int epi) {
+    if (epi == TGEMM_EPI_RELU || epi == TGEMM_EPI_BIAS_RELU) return 1;
+    if (epi == TGEMM_EPI_GELU || epi == TGEMM_EPI_BIAS_GELU) return 2;
+    return 0;
+}
+
 tgemm_status validate(const void *A, const void *B, const void *bias, const void *C, int64_t M,
                       int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int dtype,
                       int epilogue) {
@@ -113,8 +124,8 @@ tgemm_status validate(const void *A, const void *B, const void *bias, const void
     if (lda > (int64_t(1) << 40) || ldb > (int64_t(1) << 40) || ldc > (int64_t(1) << 40))
         return TGEMM_ERR_INVALID_ARG;
     if (dtype != TGEMM_F16 && dtype != TGEMM_BF16) return TGEMM_ERR_INVALID_ARG;
-    if (epilogue < TGEMM_EPI_NONE || epilogue > TGEMM_EPI_BIAS_RELU) return TGEMM_ERR_INVALID_ARG;
-    const bool use_bias = epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU;
+    if (epilogue < TGEMM_EPI_NONE || epilogue > TGEMM_EPI_BIAS_GELU) return TGEMM_ERR_INVALID_ARG;
+    const bool use_bias = uses_bias(epilogue);
     if (M == 0 || N == 0) return TGEMM_OK;
     if (C == nullptr) return TGEMM_ERR_INVALID_ARG;
     if (K > 0 && (A == nullptr || B == nullptr)) return TGEMM_ERR_INVALID_ARG;
@@ -333,8 +344,8 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
                         int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                         int dtype, int epilogue, cudaStream_t stream) {
     const bool bf16 = dtype == TGEMM_BF16;
-    const int has_bias = (epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU) ? 1 : 0;
-    const int relu = (epilogue == TGEMM_EPI_RELU || epilogue == TGEMM_EPI_BIAS_RELU) ? 1 : 0;
+    const int has_bias = uses_bias(epilogue) ? 1 : 0;
+    const int act = activation(epilogue);
     if (M == 0 || N == 0) return TGEMM_OK;
     if (K == 0) {
         const dim3 grid(static_cast<unsigned>(std::min<int64_t>(cdiv(N, 256), 64)),
@@ -342,7 +353,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
         fill_epilogue_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t *>(bias),
                                                        static_cast<uint16_t *>(C), ldc,
                                                        static_cast<int>(M), static_cast<int>(N),
-                                                       has_bias, relu, bf16 ? 1 : 0);
+                                                       has_bias, act, bf16 ? 1 : 0);
         return cudaGetLastError() == cudaSuccess ? TGEMM_OK : TGEMM_ERR_CUDA;
     }
 
@@ -397,7 +408,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     p.C = C;
     p.ldc = ldc;
     p.has_bias = has_bias;
-    p.relu = relu;
+    p.act = act;
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
@@ -465,8 +476,8 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
                                 cudaStream_t stream) {
     DeviceInfo *d = &nd->info;
     const bool bf16 = dtype == TGEMM_BF16;
-    const int has_bias = (epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU) ? 1 : 0;
-    const int relu = (epilogue == TGEMM_EPI_RELU || epilogue == TGEMM_EPI_BIAS_RELU) ? 1 : 0;
+    const int has_bias = uses_bias(epilogue) ? 1 : 0;
+    const int act = activation(epilogue);
     if (M == 0 || N == 0) return TGEMM_OK;
     if (K == 0) {
         const dim3 grid(static_cast<unsigned>(std::min<int64_t>(cdiv(N, 256), 64)),
@@ -474,7 +485,7 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
         fill_epilogue_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t *>(bias),
                                                        static_cast<uint16_t *>(C), ldc,
                                                        static_cast<int>(M), static_cast<int>(N),
-                                                       has_bias, relu, bf16 ? 1 : 0);
+                                                       has_bias, act, bf16 ? 1 : 0);
         return cudaGetLastError() == cudaSuccess ? TGEMM_OK : TGEMM_ERR_CUDA;
     }
 
@@ -526,7 +537,7 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
     p.C = C;
     p.ldc = ldc;
     p.has_bias = has_bias;
-    p.relu = relu;
+    p.act = act;
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
@@ -557,7 +568,7 @@ extern "C" tgemm_status tgemm_run_noalloc(const void *A, const void *B, const vo
     NoAllocDevice *nd = nullptr;
     if (!noalloc_setup(dev, &nd)) return TGEMM_ERR_UNSUPPORTED_DEVICE;
     if (M == 0 || N == 0) return TGEMM_OK;
-    const bool use_bias = epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU;
+    const bool use_bias = uses_bias(epilogue);
     if (!is_device_memory(C, dev) || (K > 0 && (!is_device_memory(A, dev) || !is_device_memory(B, dev))) ||
         (use_bias && !is_device_memory(bias, dev)))
         return TGEMM_ERR_INVALID_ARG;
@@ -577,7 +588,7 @@ extern "C" tgemm_status tgemm_run(const void *A, const void *B, const void *bias
     if (M == 0 || N == 0) return TGEMM_OK;
     int dev = 0;
     cudaGetDevice(&dev);
-    const bool use_bias = epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU;
+    const bool use_bias = uses_bias(epilogue);
     if (!is_device_memory(C, dev) || (K > 0 && (!is_device_memory(A, dev) || !is_device_memory(B, dev))) ||
         (use_bias && !is_device_memory(bias, dev)))
         return TGEMM_ERR_INVALID_ARG;
@@ -616,7 +627,7 @@ extern "C" tgemm_status tgemm_run_host(const void *A_host, const void *B_host,
         s_in = d->copy_in;
         s_out = d->copy_out;
     }
-    const bool use_bias = epilogue == TGEMM_EPI_BIAS || epilogue == TGEMM_EPI_BIAS_RELU;
+    const bool use_bias = uses_bias(epilogue);
     const int64_t lda_d = cdiv(K, 8) * 8, ldb_d = cdiv(N, 8) * 8, ldc_d = cdiv(N, 8) * 8;
     unsigned char *dA = nullptr, *dB = nullptr, *dbias = nullptr, *dC = nullptr;
     bool ok = true;

@@ -13,7 +13,8 @@
  * "【CUDA】TileFusion".  Precision follows the tutorial's §10.7 recipe: fp16 or
  * bf16 inputs, tensor-core products, fp32 accumulation, one final rounding to
  * the input dtype (round to nearest even).  ReLU maps x <= 0 (including -0.0)
- * to +0.0 and keeps NaN.
+ * to +0.0 and keeps NaN.  The GELU epilogue (below) is the bias + GELU fusion
+ * of "TileLang で GPU カーネル設計を解説" §4.
  *
  * Layout: every matrix is row-major with an explicit leading dimension (row
  * pitch, in elements): A[i, k] at A + i*lda + k, B[k, j] at B + k*ldb + j,
@@ -37,11 +38,18 @@ typedef struct CUstream_st *tgemm_stream_t;   /* same handle as cudaStream_t; NU
 
 typedef enum { TGEMM_F16 = 0, TGEMM_BF16 = 1 } tgemm_dtype;
 
+/*
+ * GELU is the tanh form of "TileLang で GPU カーネル設計を解説" §4, written there
+ * as a sigmoid: gelu(x) = x / (1 + exp(-1.5957691216 * (x + 0.044715 x^3))),
+ * applied after the bias; evaluated in fp32 with CUDA's fast exponential.
+ */
 typedef enum {
     TGEMM_EPI_NONE = 0,       /* C = A.B                 */
     TGEMM_EPI_RELU = 1,       /* C = max(A.B, 0)         */
     TGEMM_EPI_BIAS = 2,       /* C = A.B + bias          */
-    TGEMM_EPI_BIAS_RELU = 3   /* C = max(A.B + bias, 0)  */
+    TGEMM_EPI_BIAS_RELU = 3,  /* C = max(A.B + bias, 0)  */
+    TGEMM_EPI_GELU = 4,       /* C = gelu(A.B)           */
+    TGEMM_EPI_BIAS_GELU = 5   /* C = gelu(A.B + bias)    */
 } tgemm_epilogue;
 
 typedef enum {
@@ -59,7 +67,8 @@ typedef enum {
  * tgemm_run — enqueue C = epi(A.B + bias) on `stream` (device pointers).
  *
  * Arguments: A [M x lda], B [K x ldb], bias [N] (may be NULL unless the
- * epilogue uses it), C [M x ldc], all device pointers in `dtype`.
+ * epilogue uses it: BIAS, BIAS_RELU, BIAS_GELU), C [M x ldc], all device
+ * pointers in `dtype`.
  *
  * Errors are reported synchronously, before anything is enqueued, and leave C
  * untouched:

@@ -13,7 +13,7 @@ cross-check, and exhaustive decode / rounding checks against numpy, torch
 and a brute-force nearest-value search.
 """
 from .oracle import (  # noqa: F401
-    F16, BF16, EPI_NONE, EPI_RELU, EPI_BIAS, EPI_BIAS_RELU,
+    F16, BF16, EPI_NONE, EPI_RELU, EPI_BIAS, EPI_BIAS_RELU, EPI_GELU, EPI_BIAS_GELU,
     build, gemm_epilogue_f64, round_to, decode, max_threads, set_threads,
     dtype_code,
 )

@@ -14,11 +14,14 @@
  *    fp32 accumulation, fp16/bf16 output.
  *  - "Writing high-performance kernels in TileLang", section "Écrivons un GEMM":
  *    the activation is max(x, 0) applied to the accumulator before the store.
- *  - "TileLang で GPU カーネル設計を解説", §4: bias has shape (N,) in the input dtype.
+ *  - "TileLang で GPU カーネル設計を解説", §4: bias has shape (N,) in the input dtype;
+ *    the GELU epilogue, tanh form written as a sigmoid,
+ *    gelu(x) = x / (1 + exp(-1.5957691216 * (x + 0.044715 * x^3))), applied after
+ *    the bias (the printed bullet in "x + 0.044715·x•x·x" is read as a product).
  *
  * How: every fp16/bf16 input is decoded exactly to double; each output element
  * is the in-order fp64 sum over k of exact products, then (optionally) plus the
- * bias, then (optionally) the ReLU.  The rounding to the output dtype is a
+ * bias, then (optionally) the ReLU or the GELU.  The rounding to the output dtype is a
  * separate call (round-to-nearest-even, overflow to +-Inf), so tests can keep
  * the unrounded fp64 value for tolerance checks.  Rows run in parallel under
  * OpenMP when it is available; nothing else is reordered or blocked.
@@ -37,7 +40,13 @@
 #endif
 
 enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
-enum { ORACLE_EPI_NONE = 0, ORACLE_EPI_RELU = 1, ORACLE_EPI_BIAS = 2, ORACLE_EPI_BIAS_RELU = 3 };
+enum { ORACLE_EPI_NONE = 0, ORACLE_EPI_RELU = 1, ORACLE_EPI_BIAS = 2, ORACLE_EPI_BIAS_RELU = 3,
+       ORACLE_EPI_GELU = 4, ORACLE_EPI_BIAS_GELU = 5 };
+
+/* The tanh-form GELU as the page prints it (2*sqrt(2/pi) = 1.5957691216...). */
+static double gelu_tanh(double x) {
+    return x / (1.0 + exp(-1.5957691216 * (x + 0.044715 * x * x * x)));
+}
 
 /* Format parameters: mantissa bits (without the hidden bit), exponent bits. */
 static void fmt_params(int dtype, int *mbits, int *ebits) {
@@ -110,9 +119,11 @@ int oracle_gemm_epilogue_f64(const uint16_t *A, const uint16_t *B, const uint16_
                              int dtype, int epilogue) {
     if (M < 0 || N < 0 || K < 0 || lda < K || ldb < N) return -1;
     if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -1;
-    if (epilogue < ORACLE_EPI_NONE || epilogue > ORACLE_EPI_BIAS_RELU) return -1;
-    const int use_bias = (epilogue == ORACLE_EPI_BIAS || epilogue == ORACLE_EPI_BIAS_RELU);
+    if (epilogue < ORACLE_EPI_NONE || epilogue > ORACLE_EPI_BIAS_GELU) return -1;
+    const int use_bias = (epilogue == ORACLE_EPI_BIAS || epilogue == ORACLE_EPI_BIAS_RELU ||
+                          epilogue == ORACLE_EPI_BIAS_GELU);
     const int use_relu = (epilogue == ORACLE_EPI_RELU || epilogue == ORACLE_EPI_BIAS_RELU);
+    const int use_gelu = (epilogue == ORACLE_EPI_GELU || epilogue == ORACLE_EPI_BIAS_GELU);
     if (use_bias && bias == NULL) return -1;
     if (rows == NULL) nrows = M;
     for (int64_t r = 0; r < nrows && rows; ++r)
@@ -139,6 +150,7 @@ int oracle_gemm_epilogue_f64(const uint16_t *A, const uint16_t *B, const uint16_
             double v = acc[j];
             if (use_bias) v += decode16(bias[j], dtype);
             if (use_relu && !isnan(v) && !(v > 0.0)) v = 0.0;
+            if (use_gelu) v = gelu_tanh(v);
             acc[j] = v;
         }
     }

@@ -17,7 +17,7 @@ import threading
 import numpy as np
 
 F16, BF16 = 0, 1
-EPI_NONE, EPI_RELU, EPI_BIAS, EPI_BIAS_RELU = 0, 1, 2, 3
+EPI_NONE, EPI_RELU, EPI_BIAS, EPI_BIAS_RELU, EPI_GELU, EPI_BIAS_GELU = 0, 1, 2, 3, 4, 5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")

@@ -12,7 +12,9 @@ bias ~ N(0, 0.1), seeded):
   * B is scaled by 1/sqrt(K) and bias by 0.1 (taken as the standard deviation)
     in fp32, then everything is cast to fp16/bf16 (round to nearest even);
   * the integer-exact variant draws every entry of A, B and bias uniformly from
-    {-2, -1, 0, 1, 2} (torch.randint(-2, 3)), same order.
+    {-2, -1, 0, 1, 2} (torch.randint(-2, 3)), same order;
+  * the GELU workload follows its page's recipe ("TileLang で GPU カーネル設計を
+    解説" §4): A and B ~ N(0,1) / K^(1/4), bias ~ N(0,1), same order.
 Padded leading dimensions fill the pad with NaN so a read of the pad shows up.
 """
 from __future__ import annotations
@@ -22,7 +24,7 @@ from dataclasses import dataclass
 
 import torch
 
-EPILOGUES = {"none": 0, "relu": 1, "bias": 2, "bias_relu": 3}
+EPILOGUES = {"none": 0, "relu": 1, "bias": 2, "bias_relu": 3, "gelu": 4, "bias_gelu": 5}
 DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
 
 
@@ -56,6 +58,8 @@ WORKLOADS = {
     "c4": Workload("gemm_bias_relu_ragged_8191x6143x4104_fp16", 8191, 6143, 4104, "fp16", "bias_relu", 4),
     "c4p": Workload("gemm_bias_relu_ragged_8191x6143x4104_fp16_ld6144", 8191, 6143, 4104, "fp16",
                     "bias_relu", 4, ldb=6144, ldc=6144),
+    "c5": Workload("gemm_bias_gelu_4096x4096x1024_fp16", 4096, 4096, 1024, "fp16", "bias_gelu", 5,
+                   kind="gelu"),
 }
 
 
@@ -83,6 +87,11 @@ def make_inputs(M: int, N: int, K: int, dtype: str = "fp16", seed: int = 0,
         a = torch.randn(M, K, generator=g, dtype=torch.float32)
         b = torch.randn(K, N, generator=g, dtype=torch.float32) * (1.0 / math.sqrt(max(K, 1)))
         bias = torch.randn(N, generator=g, dtype=torch.float32) * 0.1
+    elif kind == "gelu":
+        s = 1.0 / math.sqrt(math.sqrt(max(K, 1)))
+        a = torch.randn(M, K, generator=g, dtype=torch.float32) * s
+        b = torch.randn(K, N, generator=g, dtype=torch.float32) * s
+        bias = torch.randn(N, generator=g, dtype=torch.float32)
     elif kind == "int":
         a = torch.randint(-2, 3, (M, K), generator=g).to(torch.float32)
         b = torch.randint(-2, 3, (K, N), generator=g).to(torch.float32)
@@ -96,7 +105,7 @@ def make_inputs(M: int, N: int, K: int, dtype: str = "fp16", seed: int = 0,
 
 def make_workload(w: Workload):
     """Inputs of a named workload: (A, B, bias or None)."""
-    with_bias = w.epilogue in ("bias", "bias_relu")
+    with_bias = w.epilogue in ("bias", "bias_relu", "bias_gelu")
     return make_inputs(w.M, w.N, w.K, w.dtype, w.seed, w.kind, with_bias, w.lda, w.ldb)
 
 

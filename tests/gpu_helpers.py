@@ -8,7 +8,8 @@ import torch
 import oracle
 import seeded_inputs as si
 
-EPI = {"none": 0, "relu": 1, "bias": 2, "bias_relu": 3}
+EPI = {"none": 0, "relu": 1, "bias": 2, "bias_relu": 3, "gelu": 4, "bias_gelu": 5}
+BIAS_EPIS = ("bias", "bias_relu", "bias_gelu")
 ODT = {"fp16": oracle.F16, "bf16": oracle.BF16}
 TDT = {"fp16": torch.float16, "bf16": torch.bfloat16}
 SENTINEL = 0x7E5A          # a NaN bit pattern in both fp16 and bf16; must survive in C's pad
@@ -49,7 +50,7 @@ def run_tgemm(tg, M, N, K, dtype="fp16", epilogue="bias_relu", seed=0, kind="nor
     lda = lda or K
     ldb = ldb or N
     ldc = ldc or N
-    with_bias = epilogue in ("bias", "bias_relu")
+    with_bias = epilogue in BIAS_EPIS
     A, B, bias = si.make_inputs(M, N, K, dtype, seed, kind, with_bias=True,
                                 lda=lda if lda != K else None, ldb=ldb if ldb != N else None)
     Ad = to_device_pitched(A, K) if M * K > 0 else torch.empty((M, K), dtype=TDT[dtype], device="cuda")
@@ -97,14 +98,18 @@ def magnitude(inputs, N, K, rows=None) -> np.ndarray:
     return mag.astype(np.float64)
 
 
-def assert_close(got_bits: np.ndarray, ref: np.ndarray, dtype: str, what="", mag=None, K=None):
+def assert_close(got_bits: np.ndarray, ref: np.ndarray, dtype: str, what="", mag=None, K=None,
+                 pre=None):
     """Two bounds against the unrounded fp64 oracle:
     * derived from the arithmetic (every element, any size): the fp32 sum of K
       exact products carries at most (K+2) ulp-sized errors, taken twice over
       for the tensor core's internal alignment, and one rounding to the output
       format:  |got - ref| <= u_out |ref| + (1 + u_out) 2 (K+2) 2^-24 mag + tiny;
     * the method's own statistical bounds (relative Frobenius <= 2e-3,
-      |err| <= 1e-2 + 1e-2 |ref|) when at least FROB_MIN_ELEMENTS are compared."""
+      |err| <= 1e-2 + 1e-2 |ref|) when at least FROB_MIN_ELEMENTS are compared.
+    With a GELU epilogue `pre` is the unrounded pre-activation: the sum's error
+    passes through GELU with slope at most 1.13 (taken as 1.2), and the fp32
+    evaluation of the activation adds at most 1e-5 |pre|."""
     got = decode(got_bits, dtype)
     assert got.shape == ref.shape
     finite = np.isfinite(ref)
@@ -113,7 +118,11 @@ def assert_close(got_bits: np.ndarray, ref: np.ndarray, dtype: str, what="", mag
     if mag is not None:
         gamma = 2.0 * (K + 2) * 2.0 ** -24
         u = U_OUT[dtype]
-        bound = u * np.abs(ref[finite]) + (1 + u) * gamma * mag[finite] + TINY[dtype]
+        if pre is None:
+            bound = u * np.abs(ref[finite]) + (1 + u) * gamma * mag[finite] + TINY[dtype]
+        else:
+            bound = (u * np.abs(ref[finite]) + 1.2 * (1 + u) * gamma * mag[finite]
+                     + 1e-5 * np.abs(pre[finite]) + TINY[dtype])
         bad = diff > bound
         assert not bad.any(), (f"{what}: {int(bad.sum())} elements outside the derived bound, "
                                f"worst excess {(diff - bound).max():.3e}")
@@ -142,3 +151,12 @@ def assert_bit_exact(got_bits: np.ndarray, ref: np.ndarray, dtype: str, what="")
 def assert_pad_untouched(bits_full: np.ndarray, N: int, what=""):
     if bits_full.shape[1] > N:
         assert (bits_full[:, N:] == SENTINEL).all(), f"{what}: C's pitch padding was written"
+
+
+def check_epilogue(got_bits: np.ndarray, inputs, M, N, K, dtype, epilogue, what="", rows=None):
+    """Tolerance check of any epilogue (GELU included) against the oracle."""
+    ref = oracle_ref(inputs, M, N, K, dtype, epilogue, rows=rows)
+    pre = None
+    if epilogue in ("gelu", "bias_gelu"):
+        pre = oracle_ref(inputs, M, N, K, dtype, "bias" if epilogue == "bias_gelu" else "none", rows=rows)
+    return assert_close(got_bits, ref, dtype, what, magnitude(inputs, N, K, rows), K, pre)

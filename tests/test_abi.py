@@ -54,9 +54,9 @@ def call(**kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(M=-1), INVALID), (dict(N=-1), INVALID), (dict(K=-1), INVALID),
     (dict(lda=63), INVALID), (dict(ldb=63), INVALID), (dict(ldc=63), INVALID),
-    (dict(dtype=2), INVALID), (dict(epi=4), INVALID), (dict(epi=-1), INVALID),
+    (dict(dtype=2), INVALID), (dict(epi=6), INVALID), (dict(epi=-1), INVALID),
     (dict(A=0), INVALID), (dict(B=0), INVALID), (dict(C=0), INVALID),
-    (dict(bias=0, epi=2), INVALID), (dict(bias=0, epi=3), INVALID),
+    (dict(bias=0, epi=2), INVALID), (dict(bias=0, epi=3), INVALID), (dict(bias=0, epi=5), INVALID),
     (dict(M=2 ** 31), INVALID),
     (dict(A=A + 2), ALIGN), (dict(B=B + 8), ALIGN), (dict(C=C + 2), ALIGN), (dict(bias=BIAS + 4), ALIGN),
     (dict(C=A + 64), ALIAS), (dict(C=B), ALIAS), (dict(C=BIAS - 64 * 2 + 16), ALIAS),

@@ -39,11 +39,15 @@ DTS = {oracle.F16: "fp16", oracle.BF16: "bf16"}
 
 
 def has_bias(epi):
-    return epi in (oracle.EPI_BIAS, oracle.EPI_BIAS_RELU)
+    return epi in (oracle.EPI_BIAS, oracle.EPI_BIAS_RELU, oracle.EPI_BIAS_GELU)
 
 
 def has_relu(epi):
     return epi in (oracle.EPI_RELU, oracle.EPI_BIAS_RELU)
+
+
+def has_gelu(epi):
+    return epi in (oracle.EPI_GELU, oracle.EPI_BIAS_GELU)
 
 
 # Library decoders, independent of the oracle's C decode.
@@ -263,9 +267,41 @@ def pin_nan_inf(fn):
         assert none[2, 1] == -np.inf
 
 
+def pin_gelu(fn):
+    """GELU epilogue of "TileLang で GPU カーネル設計を解説" §4 (tanh form, after the
+    bias): with A = I the pre-activation is exactly B + bias, so the output must
+    equal torch's own tanh-approximation GELU of it (a library routine written
+    with tanh, not the page's sigmoid form) to fp64 rounding; the sigmoid form
+    satisfies gelu(x) - gelu(-x) = x exactly in real arithmetic; gelu(0) = +0."""
+    rng = np.random.default_rng(13)
+    for dt in (oracle.F16, oracle.BF16):
+        K, N = 24, 40
+        eye = to_bits(np.eye(K), dt)
+        neg = to_bits(-np.eye(K), dt)
+        B = rand_bits((K, N), dt, rng, 3.0)
+        bias = rand_bits((N,), dt, rng, 1.0)
+        pre = lib_decode(B, dt) + lib_decode(bias, dt)[None, :]
+        got = fn(eye, B, bias, K, N, K, dt, oracle.EPI_BIAS_GELU)
+        lib = torch.nn.functional.gelu(torch.from_numpy(pre), approximate="tanh").numpy()
+        # The page prints 2*sqrt(2/pi) to 10 decimals (5.7e-12 short); with
+        # sigma' <= 1/4 that moves gelu by at most ~1e-12 |x| over this range.
+        assert np.all(np.abs(got - lib) <= 2e-12 * np.abs(pre) + 1e-300)
+        pos = fn(eye, B, None, K, N, K, dt, oracle.EPI_GELU)
+        negv = fn(neg, B, None, K, N, K, dt, oracle.EPI_GELU)
+        x = lib_decode(B, dt)
+        assert np.all(np.abs((pos - negv) - x) <= 4e-16 * np.abs(x))
+        zero = fn(to_bits(np.zeros((3, K)), dt), B, None, 3, N, K, dt, oracle.EPI_GELU)
+        assert np.array_equal(zero, np.zeros((3, N))) and not np.signbit(zero).any()
+        # Saturation: far right of 0 the GELU is the identity, far left it vanishes.
+        big = to_bits(np.array([[30.0], [-30.0]]), dt)
+        one = to_bits(np.ones((1, 1)), dt)
+        ends = fn(big, one, None, 2, 1, 1, dt, oracle.EPI_GELU)
+        assert ends[0, 0] == 30.0 and abs(ends[1, 0]) < 1e-300
+
+
 ALL_PINS = [pin_bruteforce_tiny, pin_identity_and_permutation, pin_zero_and_ones,
             pin_integer_exact, pin_relu_invariants, pin_linearity_homogeneity,
-            pin_fp32_library, pin_row_subset, pin_nan_inf]
+            pin_fp32_library, pin_row_subset, pin_nan_inf, pin_gelu]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
@@ -375,7 +411,8 @@ def _mut_transpose_b(A, B, bias, M, N, K, dt, epi, rows=None):
 
 
 def _mut_drop_bias(A, B, bias, M, N, K, dt, epi, rows=None):
-    e = {oracle.EPI_BIAS: oracle.EPI_NONE, oracle.EPI_BIAS_RELU: oracle.EPI_RELU}.get(epi, epi)
+    e = {oracle.EPI_BIAS: oracle.EPI_NONE, oracle.EPI_BIAS_RELU: oracle.EPI_RELU,
+         oracle.EPI_BIAS_GELU: oracle.EPI_GELU}.get(epi, epi)
     return oracle.gemm_epilogue_f64(A, B, None, M, N, K, dt, e, rows=rows)
 
 
@@ -421,8 +458,30 @@ def _mut_pitch_ignored(A, B, bias, M, N, K, dt, epi, rows=None):
     return oracle.gemm_epilogue_f64(A, B, bias, M, N, K, dt, epi, rows=rows)
 
 
+def _gelu_wrong(x, c):
+    return x / (1.0 + np.exp(-c * (x + 0.044715 * x * x * x)))
+
+
+def _mut_gelu_constant(A, B, bias, M, N, K, dt, epi, rows=None):
+    """GELU with the tanh-argument constant sqrt(2/pi) in the sigmoid form."""
+    if not has_gelu(epi):
+        return oracle.gemm_epilogue_f64(A, B, bias, M, N, K, dt, epi, rows=rows)
+    pre_epi = oracle.EPI_BIAS if has_bias(epi) else oracle.EPI_NONE
+    pre = oracle.gemm_epilogue_f64(A, B, bias, M, N, K, dt, pre_epi, rows=rows)
+    with np.errstate(over="ignore"):
+        return _gelu_wrong(pre, 0.7978845608)
+
+
+def _mut_gelu_before_bias(A, B, bias, M, N, K, dt, epi, rows=None):
+    if epi != oracle.EPI_BIAS_GELU:
+        return oracle.gemm_epilogue_f64(A, B, bias, M, N, K, dt, epi, rows=rows)
+    out = oracle.gemm_epilogue_f64(A, B, None, M, N, K, dt, oracle.EPI_GELU, rows=rows)
+    return out + oracle.decode(bias, dt)[None, :]
+
+
 MUTANTS = [_mut_transpose_b, _mut_drop_bias, _mut_bias_by_row, _mut_relu_before_bias,
-           _mut_drop_last_k, _mut_sign_flip, _mut_negative_zero, _mut_pitch_ignored]
+           _mut_drop_last_k, _mut_sign_flip, _mut_negative_zero, _mut_pitch_ignored,
+           _mut_gelu_constant, _mut_gelu_before_bias]
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=lambda m: m.__name__)
