@@ -255,8 +255,9 @@ def run_reference(args, world, rank):
 def workload_config(w):
     return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype,
             "epilogue": w.epilogue, "lda": w.lda or w.K, "ldb": w.ldb or w.N, "ldc": w.ldc or w.N,
-            "inputs": "A~N(0,1), B~N(0,1)/sqrt(K), bias~N(0,0.1)" if w.kind == "normal"
-            else "uniform integers in {-2..2}", "seed": w.seed,
+            "inputs": {"normal": "A~N(0,1), B~N(0,1)/sqrt(K), bias~N(0,0.1)",
+                       "gelu": "A, B ~N(0,1)/K^(1/4), bias~N(0,1)",
+                       "int": "uniform integers in {-2..2}"}[w.kind], "seed": w.seed,
             "l2": "flushed between steps (256 MiB write, outside the timed launch)"}
 
 
