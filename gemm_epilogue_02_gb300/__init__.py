@@ -12,8 +12,8 @@ from ._binding import (  # noqa: F401
     TGEMM_BF16, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_GELU, TGEMM_EPI_BIAS_RELU, TGEMM_EPI_GELU,
     TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_F16,
     EXPORTED, NOALLOC_SCRATCH_BYTES, STATUS, TgemmError, library_path, load,
-    tgemm_last_device_status, tgemm_run, tgemm_run_host, tgemm_run_noalloc, tgemm_status_string,
-    tgemm_version,
+    tgemm_last_device_status, tgemm_run, tgemm_run_ex, tgemm_run_host, tgemm_run_noalloc,
+    tgemm_status_string, tgemm_version,
 )
 from .build import build  # noqa: F401
 
@@ -32,16 +32,18 @@ def _check_2d(name, t):
 
 
 def run(A: torch.Tensor, B: torch.Tensor, bias, C: torch.Tensor, epilogue="bias_relu",
-        stream=None) -> torch.Tensor:
+        stream=None, transpose_a: bool = False, transpose_b: bool = False) -> torch.Tensor:
     """C = epi(A @ B + bias) on CUDA tensors, enqueued on the current (or given) stream.
 
-    A [M, K], B [K, N], C [M, N] may have row pitches wider than their widths
+    A is [M, K] (or, with transpose_a, the stored [K, M] = A^T), B is [K, N]
+    (or, with transpose_b, the stored [N, K] = B^T, the nn.Linear weight
+    layout), C is [M, N]; each may have a row pitch wider than its width
     (stride(0) >= width); bias is [N] or None.  Raises TgemmError on a status
     other than TGEMM_OK.
     """
     _check_2d("A", A), _check_2d("B", B), _check_2d("C", C)
-    M, K = A.shape
-    K2, N = B.shape
+    M, K = (A.shape[1], A.shape[0]) if transpose_a else tuple(A.shape)
+    K2, N = (B.shape[1], B.shape[0]) if transpose_b else tuple(B.shape)
     if K2 != K or tuple(C.shape) != (M, N):
         raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
     if not (A.dtype == B.dtype == C.dtype) or A.dtype not in _DT:
@@ -51,9 +53,15 @@ def run(A: torch.Tensor, B: torch.Tensor, bias, C: torch.Tensor, epilogue="bias_
         raise ValueError("bias must be a contiguous [N] tensor of the same dtype")
     s = stream if stream is not None else torch.cuda.current_stream(A.device)
     with torch.cuda.device(A.device):
-        st = tgemm_run(A.data_ptr(), B.data_ptr(), bias.data_ptr() if bias is not None else 0,
-                       C.data_ptr(), M, N, K, A.stride(0), B.stride(0), C.stride(0), _DT[A.dtype],
-                       _epi(epilogue), s.cuda_stream)
+        if transpose_a or transpose_b:
+            st = tgemm_run_ex(A.data_ptr(), B.data_ptr(), bias.data_ptr() if bias is not None else 0,
+                              C.data_ptr(), M, N, K, A.stride(0), B.stride(0), C.stride(0),
+                              _DT[A.dtype], _epi(epilogue), int(transpose_a), int(transpose_b),
+                              s.cuda_stream)
+        else:
+            st = tgemm_run(A.data_ptr(), B.data_ptr(), bias.data_ptr() if bias is not None else 0,
+                           C.data_ptr(), M, N, K, A.stride(0), B.stride(0), C.stride(0), _DT[A.dtype],
+                           _epi(epilogue), s.cuda_stream)
     if st != 0:
         raise TgemmError(st)
     return C

@@ -18,8 +18,8 @@ TGEMM_EPI_GELU, TGEMM_EPI_BIAS_GELU = 4, 5
 STATUS = {0: "TGEMM_OK", 1: "TGEMM_ERR_INVALID_ARG", 2: "TGEMM_ERR_ALIGNMENT",
           3: "TGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TGEMM_ERR_ALIAS", 5: "TGEMM_ERR_CUDA",
           6: "TGEMM_ERR_TIMEOUT", 7: "TGEMM_ERR_SCRATCH_LIMIT"}
-EXPORTED = ("tgemm_run", "tgemm_run_host", "tgemm_status_string", "tgemm_last_device_status",
-            "tgemm_version", "tgemm_run_noalloc")
+EXPORTED = ("tgemm_run", "tgemm_run_ex", "tgemm_run_host", "tgemm_status_string",
+            "tgemm_last_device_status", "tgemm_version", "tgemm_run_noalloc")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lock = threading.Lock()
@@ -52,6 +52,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p]
             f.restype = i32
+        lib.tgemm_run_ex.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, p]
+        lib.tgemm_run_ex.restype = i32
         lib.tgemm_status_string.argtypes = [i32]
         lib.tgemm_status_string.restype = ctypes.c_char_p
         lib.tgemm_last_device_status.argtypes = []
@@ -67,6 +69,14 @@ def tgemm_run(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: in
     """Raw C-ABI call with device pointers (ints); returns the status code."""
     return load().tgemm_run(A or None, B or None, bias or None, C or None, M, N, K, lda, ldb, ldc,
                             dtype, epilogue, stream or None)
+
+
+def tgemm_run_ex(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                 ldc: int, dtype: int, epilogue: int, transpose_a: int, transpose_b: int,
+                 stream: int = 0) -> int:
+    """Raw C-ABI call with either operand stored transposed; returns the status code."""
+    return load().tgemm_run_ex(A or None, B or None, bias or None, C or None, M, N, K, lda, ldb, ldc,
+                               dtype, epilogue, int(transpose_a), int(transpose_b), stream or None)
 
 
 def tgemm_run_host(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,

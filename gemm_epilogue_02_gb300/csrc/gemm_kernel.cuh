@@ -15,9 +15,11 @@
 // group of CG CTAs (CG = 1: one CTA; CG = 2: a cluster pair whose MMAs span
 // both SMs, M = 256).  In every CTA:
 //
-//   warp 0      TMA producer: its own 128 rows of A [128 x 64] (K-major) and
-//               its BN/CG columns of B [64 x BN/CG] (N-major, as sub-tiles of
-//               64 columns) per k-block into a STAGES-deep shared-memory ring,
+//   warp 0      TMA producer: its own 128 rows of A [128 x 64] and its BN/CG
+//               columns of B [64 x BN/CG] per k-block (row-major A is K-major,
+//               row-major B is N-major in 64-column sub-tiles; either operand
+//               may instead be stored transposed, which flips its major
+//               dimension) into a STAGES-deep shared-memory ring,
 //               128-byte swizzled.  The stage's full barrier lives in CTA rank 0
 //               and counts the bytes of both CTAs (rank 0 announces them all;
 //               the peer's copies report there); each CTA's empty barrier is
@@ -72,6 +74,9 @@ struct KParams {
     void *C;                   // used by the masked-store path only
     long long ldc;
     int has_bias, act, is_bf16, tma_store;   // act: 0 none, 1 ReLU, 2 GELU
+    int a_mn;                  // A stored transposed ([K, M], M contiguous): MN-major operand
+    int b_kmajor;              // B stored transposed ([N, K], K contiguous): K-major operand
+    uint32_t stage_tx;         // bytes one CTA loads per ring stage (depends on the layouts)
     uint32_t idesc;
     unsigned int *status;      // device status word
 };
@@ -250,23 +255,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     const uint32_t a_dst = sbase + L::kOffA + stage * L::kABytes;
                     const uint32_t b_dst = sbase + L::kOffB + stage * L::kBBytes;
-                    if constexpr (CG == 1) {
-                        const uint32_t fb = full_bar(stage);
-                        mbar_arrive_expect_tx(fb, L::kStageTx);
-                        tma_load_2d(a_dst, &tmA, fb, kb * kBK, a_row);
-#pragma unroll
-                        for (int j = 0; j < L::kBSub; ++j)
-                            tma_load_2d(b_dst + j * (kBK * 128), &tmB, fb, b_col + j * 64, kb * kBK);
+                    // Rank 0 announces the bytes of the whole group; with a CTA pair the
+                    // peer's copies report to rank 0's barrier (its transaction count may
+                    // dip below zero until the announcement lands, which is allowed).
+                    const uint32_t fb = (CG == 1) ? full_bar(stage) : leader_full(stage);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), CG * p.stage_tx);
+                    auto load = [&](uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y) {
+                        if constexpr (CG == 1) tma_load_2d(dst, m, fb, x, y);
+                        else tma_load_2d_pair(dst, m, fb, x, y);
+                    };
+                    if (!p.a_mn) {
+                        // A [M, K]: one box of 128 rows x 64 k (K-major, 128-byte rows).
+                        load(a_dst, &tmA, kb * kBK, a_row);
                     } else {
-                        // Rank 0 announces the bytes of both CTAs; the peer's copies
-                        // report to rank 0's barrier (its transaction count may dip
-                        // below zero until the announcement lands, which is allowed).
-                        const uint32_t fb = leader_full(stage);
-                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), CG * L::kStageTx);
-                        tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, a_row);
+                        // A stored [K, M]: two boxes of 64 k-rows x 64 m (MN-major).
+#pragma unroll
+                        for (int j = 0; j < kBM / 64; ++j)
+                            load(a_dst + j * (kBK * 128), &tmA, a_row + j * 64, kb * kBK);
+                    }
+                    if (!p.b_kmajor) {
+                        // B [K, N]: 64-column sub-tiles of 64 k-rows (MN-major).
 #pragma unroll
                         for (int j = 0; j < L::kBSub; ++j)
-                            tma_load_2d_pair(b_dst + j * (kBK * 128), &tmB, fb, b_col + j * 64, kb * kBK);
+                            load(b_dst + j * (kBK * 128), &tmB, b_col + j * 64, kb * kBK);
+                    } else {
+                        // B stored [N, K]: one box of BN/CG n-rows x 64 k (K-major).
+                        load(b_dst, &tmB, kb * kBK, b_col);
                     }
                     ++uses[stage];
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -304,11 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b_addr = sbase + L::kOffB + stage * L::kBBytes;
 #pragma unroll
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        // A: K-major, 8-row groups 1 KiB apart; a 16-wide k step is 32 B along the row.
-                        const uint64_t adesc = sw128_desc(a_addr + k * (kUmmaK * 2), 16, 1024);
-                        // B: N-major; 64-column sub-tiles kBK*128 B apart (leading), 8-row k groups
-                        // 1 KiB apart (stride); a 16-wide k step is 16 rows = 2 KiB.
-                        const uint64_t bdesc = sw128_desc(b_addr + k * (kUmmaK * 128), kBK * 128, 1024);
+                        // K-major operand: 8-row groups 1 KiB apart (stride); a 16-wide k step
+                        // is 32 B along the 128-byte row.  MN-major operand: 64-element
+                        // sub-tiles kBK*128 B apart (leading), 8-row k groups 1 KiB apart
+                        // (stride); a 16-wide k step is 16 rows = 2 KiB.
+                        const uint64_t adesc = p.a_mn ? sw128_desc(a_addr + k * (kUmmaK * 128), kBK * 128, 1024)
+                                                      : sw128_desc(a_addr + k * (kUmmaK * 2), 16, 1024);
+                        const uint64_t bdesc = p.b_kmajor ? sw128_desc(b_addr + k * (kUmmaK * 2), 16, 1024)
+                                                          : sw128_desc(b_addr + k * (kUmmaK * 128), kBK * 128, 1024);
                         mma_f16_ss<CG>(d_tmem, adesc, bdesc, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit<CG>(empty_bar(stage));      // frees the ring stage once read

@@ -115,12 +115,17 @@ int activation(int epi) {
     return 0;
 }
 
+// ta / tb: A stored as [K, M] / B stored as [N, K] (transposed), else row-major
+// A [M, K] / B [K, N]; lda / ldb are the pitches of the stored matrices.
 tgemm_status validate(const void *A, const void *B, const void *bias, const void *C, int64_t M,
                       int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int dtype,
-                      int epilogue) {
+                      int epilogue, int ta = 0, int tb = 0) {
     if (M < 0 || N < 0 || K < 0) return TGEMM_ERR_INVALID_ARG;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return TGEMM_ERR_INVALID_ARG;
-    if (lda < K || ldb < N || ldc < N) return TGEMM_ERR_INVALID_ARG;
+    if ((ta != 0 && ta != 1) || (tb != 0 && tb != 1)) return TGEMM_ERR_INVALID_ARG;
+    const int64_t a_rows = ta ? K : M, a_cols = ta ? M : K;
+    const int64_t b_rows = tb ? N : K, b_cols = tb ? K : N;
+    if (lda < a_cols || ldb < b_cols || ldc < N) return TGEMM_ERR_INVALID_ARG;
     if (lda > (int64_t(1) << 40) || ldb > (int64_t(1) << 40) || ldc > (int64_t(1) << 40))
         return TGEMM_ERR_INVALID_ARG;
     if (dtype != TGEMM_F16 && dtype != TGEMM_BF16) return TGEMM_ERR_INVALID_ARG;
@@ -134,7 +139,7 @@ tgemm_status validate(const void *A, const void *B, const void *bias, const void
         (use_bias && !aligned16(bias)))
         return TGEMM_ERR_ALIGNMENT;
     const Range rc = span(C, M, ldc, N);
-    if (K > 0 && (overlaps(rc, span(A, M, lda, K)) || overlaps(rc, span(B, K, ldb, N))))
+    if (K > 0 && (overlaps(rc, span(A, a_rows, lda, a_cols)) || overlaps(rc, span(B, b_rows, ldb, b_cols))))
         return TGEMM_ERR_ALIAS;
     if (use_bias && overlaps(rc, span(bias, 1, N, N))) return TGEMM_ERR_ALIAS;
     return TGEMM_OK;
@@ -318,7 +323,8 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
     int group_m = 16;
     if (const char *g = std::getenv("TGEMM_GROUP_M")) group_m = std::max(1, std::atoi(g));
     p.group_m = std::min(p.num_m, group_m);
-    p.idesc = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(cfg.bn), false, true);
+    p.idesc = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(cfg.bn),
+                        p.a_mn != 0, p.b_kmajor == 0);
     switch (cfg.bit) {
         case 1: return launch_fused<256, 4, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
         case 2: return launch_fused<128, 6, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
@@ -340,9 +346,30 @@ cudaError_t repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t
     return cudaGetLastError();
 }
 
+// Tensor maps of A, B (for their stored layouts, 16-byte pitches) and C for
+// configuration `cfg`; fills the layout fields of p.  A stored [M, K]: boxes of
+// 128 rows x 64 k; stored [K, M]: 64 k-rows x 64 m.  B stored [K, N]: 64 k-rows
+// x 64 n; stored [N, K]: BN/CG n-rows x 64 k.  C: 32 rows x the chunk width.
+bool encode_maps(const Cfg &cfg, const void *a, int64_t lda, int ta, const void *b, int64_t ldb, int tb,
+                 void *C, int64_t ldc, bool tma_store, int64_t M, int64_t N, int64_t K, bool bf16,
+                 CUtensorMap *tma, CUtensorMap *tmb, CUtensorMap *tmc, KParams *p) {
+    const int bcols = cfg.bn / cfg.cg;
+    std::memset(tmc, 0, sizeof(*tmc));
+    const bool ok =
+        (ta ? make_map(tma, a, K, M, lda, 64, kBK, bf16) : make_map(tma, a, M, K, lda, kBK, kBM, bf16)) &&
+        (tb ? make_map(tmb, b, N, K, ldb, kBK, static_cast<uint32_t>(bcols), bf16)
+            : make_map(tmb, b, K, N, ldb, 64, kBK, bf16)) &&
+        (!tma_store || make_map(tmc, C, M, N, ldc, static_cast<uint32_t>(cfg.cw()), 32, bf16));
+    p->a_mn = ta;
+    p->b_kmajor = tb;
+    p->stage_tx = static_cast<uint32_t>(kBM * kBK * 2 +
+                                        (tb ? bcols * kBK * 2 : cdiv(bcols, 64) * 64 * kBK * 2));
+    return ok;
+}
+
 tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void *bias, void *C,
                         int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                        int dtype, int epilogue, cudaStream_t stream) {
+                        int dtype, int epilogue, cudaStream_t stream, int ta = 0, int tb = 0) {
     const bool bf16 = dtype == TGEMM_BF16;
     const int has_bias = uses_bias(epilogue) ? 1 : 0;
     const int act = activation(epilogue);
@@ -366,19 +393,21 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
         if (scratch_a) cudaFreeAsync(scratch_a, stream);
         if (scratch_b) cudaFreeAsync(scratch_b, stream);
     };
+    const int64_t a_rows = ta ? K : M, a_cols = ta ? M : K;
+    const int64_t b_rows = tb ? N : K, b_cols = tb ? K : N;
     if (lda % 8 != 0) {
-        lda_use = cdiv(K, 8) * 8;
-        if (cudaMallocFromPoolAsync(&scratch_a, static_cast<size_t>(M * lda_use * 2), d->pool,
+        lda_use = cdiv(a_cols, 8) * 8;
+        if (cudaMallocFromPoolAsync(&scratch_a, static_cast<size_t>(a_rows * lda_use * 2), d->pool,
                                     stream) != cudaSuccess ||
-            repack(A, lda, scratch_a, lda_use, M, K, stream) != cudaSuccess)
+            repack(A, lda, scratch_a, lda_use, a_rows, a_cols, stream) != cudaSuccess)
             st = TGEMM_ERR_CUDA;
         a_use = scratch_a;
     }
     if (st == TGEMM_OK && ldb % 8 != 0) {
-        ldb_use = cdiv(N, 8) * 8;
-        if (cudaMallocFromPoolAsync(&scratch_b, static_cast<size_t>(K * ldb_use * 2), d->pool,
+        ldb_use = cdiv(b_cols, 8) * 8;
+        if (cudaMallocFromPoolAsync(&scratch_b, static_cast<size_t>(b_rows * ldb_use * 2), d->pool,
                                     stream) != cudaSuccess ||
-            repack(B, ldb, scratch_b, ldb_use, K, N, stream) != cudaSuccess)
+            repack(B, ldb, scratch_b, ldb_use, b_rows, b_cols, stream) != cudaSuccess)
             st = TGEMM_ERR_CUDA;
         b_use = scratch_b;
     }
@@ -390,17 +419,14 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
 
     const Cfg cfg = choose_config(M, N, d->num_sms);
     const bool tma_store = (ldc % 8) == 0;
-    CUtensorMap ta, tb, tc;
-    std::memset(&tc, 0, sizeof(tc));
-    if (!make_map(&ta, a_use, M, K, lda_use, kBK, kBM, bf16) ||
-        !make_map(&tb, b_use, K, N, ldb_use, 64, kBK, bf16) ||
-        (tma_store && !make_map(&tc, C, M, N, ldc, cfg.cw(), 32, bf16))) {
+    CUtensorMap tma, tmb, tmc;
+    KParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!encode_maps(cfg, a_use, lda_use, ta, b_use, ldb_use, tb, C, ldc, tma_store, M, N, K, bf16,
+                     &tma, &tmb, &tmc, &p)) {
         release();
         return TGEMM_ERR_CUDA;
     }
-
-    KParams p;
-    std::memset(&p, 0, sizeof(p));
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
@@ -412,7 +438,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
-    const cudaError_t e = launch_config(d, cfg, ta, tb, tc, p, stream, bf16);
+    const cudaError_t e = launch_config(d, cfg, tma, tmb, tmc, p, stream, bf16);
     release();
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -521,15 +547,12 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
 
     const Cfg cfg = choose_config(M, N, d->num_sms);
     const bool tma_store = (ldc % 8) == 0;
-    CUtensorMap ta, tb, tc;
-    std::memset(&tc, 0, sizeof(tc));
-    if (!make_map(&ta, a_use, M, K, lda_use, kBK, kBM, bf16) ||
-        !make_map(&tb, b_use, K, N, ldb_use, 64, kBK, bf16) ||
-        (tma_store && !make_map(&tc, C, M, N, ldc, cfg.cw(), 32, bf16)))
-        return TGEMM_ERR_CUDA;
-
+    CUtensorMap tma, tmb, tmc;
     KParams p;
     std::memset(&p, 0, sizeof(p));
+    if (!encode_maps(cfg, a_use, lda_use, 0, b_use, ldb_use, 0, C, ldc, tma_store, M, N, K, bf16, &tma,
+                     &tmb, &tmc, &p))
+        return TGEMM_ERR_CUDA;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
@@ -541,7 +564,7 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
-    const cudaError_t e = launch_config(d, cfg, ta, tb, tc, p, stream, bf16);
+    const cudaError_t e = launch_config(d, cfg, tma, tmb, tmc, p, stream, bf16);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return TGEMM_ERR_CUDA;
@@ -576,11 +599,12 @@ extern "C" tgemm_status tgemm_run_noalloc(const void *A, const void *B, const vo
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" tgemm_status tgemm_run(const void *A, const void *B, const void *bias, void *C,
-                                  int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                                  int64_t ldc, tgemm_dtype dtype, tgemm_epilogue epilogue,
-                                  tgemm_stream_t stream) {
-    tgemm_status st = validate(A, B, bias, C, M, N, K, lda, ldb, ldc, dtype, epilogue);
+extern "C" tgemm_status tgemm_run_ex(const void *A, const void *B, const void *bias, void *C,
+                                     int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                     int64_t ldc, tgemm_dtype dtype, tgemm_epilogue epilogue,
+                                     int transpose_a, int transpose_b, tgemm_stream_t stream) {
+    tgemm_status st = validate(A, B, bias, C, M, N, K, lda, ldb, ldc, dtype, epilogue, transpose_a,
+                               transpose_b);
     if (st != TGEMM_OK) return st;
     DeviceInfo *d = nullptr;
     st = current_device(&d);
@@ -593,7 +617,14 @@ extern "C" tgemm_status tgemm_run(const void *A, const void *B, const void *bias
         (use_bias && !is_device_memory(bias, dev)))
         return TGEMM_ERR_INVALID_ARG;
     return run_device(d, A, B, bias, C, M, N, K, lda, ldb, ldc, dtype, epilogue,
-                      reinterpret_cast<cudaStream_t>(stream));
+                      reinterpret_cast<cudaStream_t>(stream), transpose_a, transpose_b);
+}
+
+extern "C" tgemm_status tgemm_run(const void *A, const void *B, const void *bias, void *C,
+                                  int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                  int64_t ldc, tgemm_dtype dtype, tgemm_epilogue epilogue,
+                                  tgemm_stream_t stream) {
+    return tgemm_run_ex(A, B, bias, C, M, N, K, lda, ldb, ldc, dtype, epilogue, 0, 0, stream);
 }
 
 // End-to-end call on host buffers.  The device copies use compact 16-byte

@@ -100,6 +100,27 @@ tgemm_status tgemm_run(const void *A, const void *B, const void *bias, void *C,
                        tgemm_dtype dtype, tgemm_epilogue epilogue, tgemm_stream_t stream);
 
 /*
+ * tgemm_run_ex — tgemm_run with either operand stored transposed (the
+ * transpose_A / transpose_B options of T.gemm in "Writing high-performance
+ * kernels in TileLang", "Écrivons un GEMM"; the column-major B of
+ * "【CUDA】TileFusion").  The product is still C = epi(A.B + bias) with A
+ * M x K and B K x N:
+ *   transpose_a = 0: A[i, k] at A + i*lda + k   (stored [M, lda], lda >= K)
+ *   transpose_a = 1: A[i, k] at A + k*lda + i   (stored [K, lda], lda >= M)
+ *   transpose_b = 0: B[k, j] at B + k*ldb + j   (stored [K, ldb], ldb >= N)
+ *   transpose_b = 1: B[k, j] at B + j*ldb + k   (stored [N, ldb], ldb >= K:
+ *                    the [out_features, in_features] weight layout)
+ * The tensor cores read either major directly; nothing is transposed in
+ * memory.  Errors as tgemm_run (a transpose flag other than 0 or 1 ->
+ * TGEMM_ERR_INVALID_ARG).
+ */
+tgemm_status tgemm_run_ex(const void *A, const void *B, const void *bias, void *C,
+                          int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int64_t ldc,
+                          tgemm_dtype dtype, tgemm_epilogue epilogue,
+                          int transpose_a, int transpose_b, tgemm_stream_t stream);
+
+/*
  * tgemm_run_host — the same operation on HOST buffers (pinned or pageable),
  * end to end: device buffers are drawn from the library's stream-ordered pool,
  * A, B and bias are copied host -> device on `stream`, tgemm_run is enqueued,

@@ -160,3 +160,26 @@ def check_epilogue(got_bits: np.ndarray, inputs, M, N, K, dtype, epilogue, what=
     if epilogue in ("gelu", "bias_gelu"):
         pre = oracle_ref(inputs, M, N, K, dtype, "bias" if epilogue == "bias_gelu" else "none", rows=rows)
     return assert_close(got_bits, ref, dtype, what, magnitude(inputs, N, K, rows), K, pre)
+
+
+def run_tgemm_layout(tg, M, N, K, dtype="fp16", epilogue="bias_relu", seed=0, kind="normal",
+                     transpose_a=False, transpose_b=False, pad_a=0, pad_b=0):
+    """Like run_tgemm, with A stored as [K, M] (transpose_a) and/or B stored as
+    [N, K] (transpose_b), each with `pad_*` extra (NaN) columns of pitch.
+    Returns the logical (A [M, K], B [K, N], bias) inputs and C's bits."""
+    A, B, bias = si.make_inputs(M, N, K, dtype, seed, kind, with_bias=True)
+    def stored(x, transpose, pad):
+        x = x.t().contiguous() if transpose else x
+        if pad:
+            full = torch.full((x.shape[0], x.shape[1] + pad), float("nan"), dtype=x.dtype)
+            full[:, : x.shape[1]] = x
+            x = full
+        return x.to("cuda")[:, : (x.shape[1] - pad)]
+    Ad = stored(A, transpose_a, pad_a)
+    Bd = stored(B, transpose_b, pad_b)
+    with_bias = epilogue in BIAS_EPIS
+    Cd = alloc_c(M, N, N, dtype)
+    tg.run(Ad, Bd, bias.to("cuda") if with_bias else None, Cd, epilogue,
+           transpose_a=transpose_a, transpose_b=transpose_b)
+    torch.cuda.synchronize()
+    return (A, B, bias if with_bias else None), c_bits(Cd, M, N)

@@ -83,3 +83,20 @@ def test_valid_call_without_gpu_reports_unsupported_device():
     buf = (ctypes.c_uint16 * 64)()
     p = ctypes.addressof(buf)
     assert tg.tgemm_run_host(p, p + 32, 0, p + 64, 4, 4, 4, 4, 4, 4, 0, 1, 0) in (UNSUPPORTED, ALIAS)
+
+
+def call_ex(ta, tb, **kw):
+    args = dict(A=A, B=B, bias=BIAS, C=C, M=64, N=32, K=48, lda=64, ldb=48, ldc=32)
+    args.update(kw)
+    return tg.tgemm_run_ex(args["A"], args["B"], args["bias"], args["C"], args["M"], args["N"], args["K"],
+                           args["lda"], args["ldb"], args["ldc"], 0, 3, ta, tb, 0)
+
+
+def test_transposed_layout_validation():
+    # Stored [K, M] A needs lda >= M; stored [N, K] B needs ldb >= K.
+    assert call_ex(1, 1, lda=63) == INVALID
+    assert call_ex(1, 1, ldb=47) == INVALID
+    assert call_ex(2, 0) == INVALID
+    assert call_ex(0, -1, lda=48, ldb=32) == INVALID
+    assert call_ex(1, 1) in (OK, UNSUPPORTED)
+    assert call_ex(0, 0, lda=48, ldb=32) in (OK, UNSUPPORTED)

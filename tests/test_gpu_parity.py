@@ -19,7 +19,7 @@ import torch
 import oracle
 import seeded_inputs as si
 from gpu_helpers import (EPI, assert_bit_exact, assert_close, assert_pad_untouched, c_bits,
-                         check_epilogue, magnitude, oracle_ref, run_tgemm)
+                         check_epilogue, magnitude, oracle_ref, run_tgemm, run_tgemm_layout)
 
 pytestmark = pytest.mark.gpu
 
@@ -143,6 +143,40 @@ def test_pair_rows_beyond_m(cuda_lib, monkeypatch, cfg):
     for (M, N, K) in [(128, 520, 300), (100, 64, 64), (300, 100, 130), (1, 1, 1)]:
         inputs, got = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=M + N, kind="int")
         assert_bit_exact(got, oracle_ref(inputs, M, N, K, "fp16", "bias_relu"), "fp16", f"{cfg} {M}x{N}x{K}")
+
+
+# ------------------------------------------------------------------ layouts
+@pytest.mark.parametrize("ta,tb", [(0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("cfg", CONFIGS)
+def test_transposed_operands(cuda_lib, monkeypatch, cfg, ta, tb):
+    """A stored [K, M] and/or B stored [N, K] (the T.gemm transpose options,
+    the nn.Linear weight layout): ragged M / N / K, every tile configuration."""
+    monkeypatch.setenv("TGEMM_FORCE_CFG", cfg)
+    M, N, K = 333, 700, 1000
+    inputs, got = run_tgemm_layout(cuda_lib, M, N, K, "bf16", "bias_relu", seed=31, kind="int",
+                                   transpose_a=bool(ta), transpose_b=bool(tb))
+    assert_bit_exact(got, oracle_ref(inputs, M, N, K, "bf16", "bias_relu"), "bf16", f"{cfg} ta={ta} tb={tb}")
+    inputs, got = run_tgemm_layout(cuda_lib, M, N, K, "fp16", "bias_gelu", seed=32, kind="gelu",
+                                   transpose_a=bool(ta), transpose_b=bool(tb))
+    check_epilogue(got, inputs, M, N, K, "fp16", "bias_gelu", f"{cfg} ta={ta} tb={tb}")
+
+
+@pytest.mark.parametrize("ta,tb,pad_a,pad_b", [(1, 1, 3, 5), (0, 1, 0, 1), (1, 0, 7, 0)])
+def test_transposed_operands_unaligned_pitch(cuda_lib, ta, tb, pad_a, pad_b):
+    """Transposed storage whose pitch is not a multiple of 8 goes through the repack."""
+    M, N, K = 257, 300, 129
+    inputs, got = run_tgemm_layout(cuda_lib, M, N, K, "fp16", "bias", seed=33, kind="int",
+                                   transpose_a=bool(ta), transpose_b=bool(tb), pad_a=pad_a, pad_b=pad_b)
+    assert_bit_exact(got, oracle_ref(inputs, M, N, K, "fp16", "bias"), "fp16", "pitch")
+
+
+def test_linear_layout_4096(cuda_lib):
+    """The 4096^3 workload with B in the [out_features, in_features] layout."""
+    w = si.WORKLOADS["c1"]
+    inputs, got = run_tgemm_layout(cuda_lib, w.M, w.N, w.K, w.dtype, w.epilogue, w.seed,
+                                   transpose_b=True)
+    rows = sample_rows(w.M, n=16, seed=3)
+    check_epilogue(got[rows], inputs, w.M, w.N, w.K, w.dtype, w.epilogue, "c1 B^T", rows=rows)
 
 
 # ------------------------------------------------------------------ degenerate
