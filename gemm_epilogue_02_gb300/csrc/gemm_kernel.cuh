@@ -66,6 +66,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;   // producer, MMA, epilogue warps
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kPeerCopyGraceNs = 200000ull;   // 200 us for in-flight copies on abort
 constexpr uint32_t kStatusTimeout = 6;             // TGEMM_ERR_TIMEOUT
+constexpr uint32_t kStatusLaunch = 5;              // TGEMM_ERR_CUDA: unexpected launch layout
 
 struct KParams {
     int M, N, K;
@@ -74,12 +75,31 @@ struct KParams {
     void *C;                   // used by the masked-store path only
     long long ldc;
     int has_bias, act, is_bf16, tma_store;   // act: 0 none, 1 ReLU, 2 GELU
+    int direct_store;          // 1: full chunks go straight from registers to C (16-byte rows)
     int a_mn;                  // A stored transposed ([K, M], M contiguous): MN-major operand
     int b_kmajor;              // B stored transposed ([N, K], K contiguous): K-major operand
     uint32_t stage_tx;         // bytes one CTA loads per ring stage (depends on the layouts)
     uint32_t idesc;
     unsigned int *status;      // device status word
+#ifdef TGEMM_TRACE
+    unsigned long long *trace; // timeline stamps of the first CTAs (trace builds only)
+#endif
 };
+
+// Trace builds only (-DTGEMM_TRACE): %globaltimer stamps of CTAs 0..7 into
+// p.trace[cta * 64 + slot].  Slots: 0 entry, 1 set-up done, 2 teardown start,
+// 3 exit; per tile i < 8: 8+4i first MMA issued, 9+4i last MMA committed,
+// 10+4i epilogue start (warp 2), 11+4i epilogue stores issued (warp 2).
+#ifdef TGEMM_TRACE
+#define TGEMM_STAMP(slot)                                                                         \
+    do {                                                                                          \
+        if (blockIdx.x < 8 && (slot) < 64) p.trace[blockIdx.x * 64 + (slot)] = globaltimer_ns(); \
+    } while (0)
+#else
+#define TGEMM_STAMP(slot) \
+    do {                  \
+    } while (0)
+#endif
 
 template <int BN, int STAGES, int CG>
 struct Smem {
@@ -93,16 +113,22 @@ struct Smem {
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
     static constexpr uint32_t kOffC = kOffB + STAGES * kBBytes;
-    // Staging buffers per epilogue warp: two when they fit, else one.
+    // Per epilogue warp: its tile's bias columns (16-bit, at most half of BN
+    // rounded up to whole chunks), then its C staging buffers (two when they fit).
+    static constexpr uint32_t kBiasCols = ((BN / kCW + 1) / 2) * kCW;
+    static constexpr uint32_t kOffBias = kOffC;
+    static constexpr uint32_t kOffCStage = kOffBias + ((kEpiWarps * kBiasCols * 2 + 1023) / 1024) * 1024;
     static constexpr uint32_t kCBufs =
-        (kOffC + kEpiWarps * 2 * kCStageBytes + 2048 <= 232448) ? 2 : 1;
-    static constexpr uint32_t kOffBar = kOffC + kEpiWarps * kCBufs * kCStageBytes;
+        (kOffCStage + kEpiWarps * 2 * kCStageBytes + 1024 <= 232448) ? 2 : 1;
+    static constexpr uint32_t kOffBar = kOffCStage + kEpiWarps * kCBufs * kCStageBytes;
     // full[S], empty[S], tfull[2], tempty[2], drain
     static constexpr uint32_t kNumBars = 2 * STAGES + 5;
     static constexpr uint32_t kOffTmemHolder = kOffBar + kNumBars * 8;
     static constexpr uint32_t kOffAbort = kOffTmemHolder + 4;
     static constexpr uint32_t kBytes = kOffAbort + 4;
-    static constexpr uint32_t kDynamicBytes = kBytes + 1024;   // 1 KiB alignment slack
+    // The dynamic shared memory base is 1 KiB aligned (it follows the driver's
+    // 1 KiB reserve); the kernel checks this at entry instead of keeping slack.
+    static constexpr uint32_t kDynamicBytes = kBytes;
     // Accumulator a starts at TMEM column a * kAccStride (a power of two >= BN).
     static constexpr uint32_t kAccStride = (BN <= 32) ? 32 : (BN <= 64) ? 64 : (BN <= 128) ? 128 : 256;
     static constexpr uint32_t kTmemCols = (2 * kAccStride < 32) ? 32 : 2 * kAccStride;
@@ -110,7 +136,7 @@ struct Smem {
     static_assert(BN % 32 == 0 && kBCols % 16 == 0, "tile width");
     static_assert(kTmemCols <= 512, "two accumulators must fit in TMEM");
     static_assert(kDynamicBytes <= 232448, "shared memory budget exceeded");
-    static_assert(kOffB % 1024 == 0 && kOffC % 1024 == 0, "swizzled buffers need 1 KiB alignment");
+    static_assert(kOffB % 1024 == 0 && kOffCStage % 1024 == 0, "swizzled buffers need 1 KiB alignment");
 };
 
 // Bounded wait.  Returns false if the CTA is aborting or the limit ran out.
@@ -187,10 +213,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tgemm_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const KParams p) {
     using L = Smem<BN, STAGES, CG>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
+    // Swizzled TMA tiles need a 1 KiB-aligned base.  The same for every CTA, so
+    // all threads (and both CTAs of a pair) leave together before any barrier.
+    if (sbase & 1023u) {
+        if (threadIdx.x == 0) atomicExch(p.status, kStatusLaunch);
+        return;
+    }
     const uint32_t bar0 = sbase + L::kOffBar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -202,6 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) TGEMM_STAMP(0);
+#ifdef TGEMM_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < 8) p.trace[blockIdx.x * 64 + 4] = smem_u32(smem_raw);
+#endif
     const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
     const int group_id = (CG == 2) ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
     const int num_groups = (CG == 2) ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
@@ -237,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    if (threadIdx.x == 0) TGEMM_STAMP(1);
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -307,13 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = group_id; t < p.num_tiles && ok; t += num_groups) {
+            int tile_i = 0;
+            for (int t = group_id; t < p.num_tiles && ok; t += num_groups, ++tile_i) {
                 if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * L::kAccStride;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bar(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
+                    if (kb == 0 && tile_i < 8) TGEMM_STAMP(8 + 4 * tile_i);
                     const uint32_t a_addr = sbase + L::kOffA + stage * L::kABytes;
                     const uint32_t b_addr = sbase + L::kOffB + stage * L::kBBytes;
 #pragma unroll
@@ -333,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 mma_commit<CG>(tfull_bar(acc));            // accumulator ready for the epilogue
+                if (tile_i < 8) TGEMM_STAMP(9 + 4 * tile_i);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             // All MMAs issued by this thread complete before TMEM is released.
@@ -349,8 +388,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         int buf = 0;
-        const uint32_t cstage0 = sbase + L::kOffC + ew * L::kCBufs * L::kCStageBytes;
-        uint8_t *cstage_gen0 = smem + L::kOffC + ew * L::kCBufs * L::kCStageBytes;
+        const uint32_t cstage0 = sbase + L::kOffCStage + ew * L::kCBufs * L::kCStageBytes;
+        uint8_t *cstage_gen0 = smem + L::kOffCStage + ew * L::kCBufs * L::kCStageBytes;
+        // This warp's bias strip (16-bit values): entry i is column
+        // (part + 2 * (i / CW)) * CW + i % CW of the tile.
+        unsigned short *bias_s = reinterpret_cast<unsigned short *>(smem + L::kOffBias) + ew * L::kBiasCols;
+        constexpr int kBiasPerLane = (L::kBiasCols + 31) / 32;
+        unsigned short bias_next[kBiasPerLane];
+        // Loads (into registers) the bias columns this warp needs for tile t.
+        auto fetch_bias = [&](int t) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+#pragma unroll
+            for (int k = 0; k < kBiasPerLane; ++k) {
+                const int i = lane + 32 * k;
+                const int col = nb * BN + (part + 2 * (i / CW)) * CW + i % CW;
+                bias_next[k] = (p.has_bias && i < static_cast<int>(L::kBiasCols) && col < p.N &&
+                                (part + 2 * (i / CW)) * CW < BN)
+                                   ? __ldg(reinterpret_cast<const unsigned short *>(p.bias) + col)
+                                   : static_cast<unsigned short>(0);   // +0.0 in fp16 and bf16
+            }
+        };
+        if (group_id < p.num_tiles) fetch_bias(group_id);
         // Staging swizzle, matching the C tensor map: 16-byte chunk j of row r
         // sits at j ^ (r % 8) for 128-byte rows and j ^ ((r / 2) % 4) for 64-byte rows.
         auto swz = [](int row) { return (CW == 64) ? (row & 7) : ((row >> 1) & 3); };
@@ -362,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else mbar_arrive_cluster(leader_tempty(a));
             }
         };
-        for (int t = group_id; t < p.num_tiles; t += num_groups) {
+        int tile_i = 0;
+        for (int t = group_id; t < p.num_tiles; t += num_groups, ++tile_i) {
             int m_blk, n_blk;
             tile_coords(t, p, m_blk, n_blk);
             int ok = 1;
@@ -370,6 +430,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
+            if (warp == 2 && lane == 0 && tile_i < 8) TGEMM_STAMP(10 + 4 * tile_i);
+            // Publish this tile's bias strip, then start fetching the next tile's.
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < kBiasPerLane; ++k)
+                if (lane + 32 * k < static_cast<int>(L::kBiasCols)) bias_s[lane + 32 * k] = bias_next[k];
+            __syncwarp();
+            if (t + num_groups < p.num_tiles) fetch_bias(t + num_groups);
             const int m0 = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM + q * 32;
             const int n_tile = n_blk * BN;
             // Only chunks / rows that intersect C are read out and stored (no
@@ -392,37 +460,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int H = decltype(hc)::value;
                 const int c = chunk_of(sub);
                 const int n0 = n_tile + c * CW;
-                const int nh = n0 + 32 * H;
-                const bool full_bias = p.has_bias && (nh + 32 <= p.N);
+                // Bias of these 32 columns from the warp's strip (broadcast reads).
+                const uint4 *bsrc = reinterpret_cast<const uint4 *>(bias_s + ((sub / SUBS) * CW + 32 * H));
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
+                    const uint4 raw = bsrc[g];
+                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
                     float bv[8];
-                    if (full_bias) {
-                        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-                                                    reinterpret_cast<const unsigned short *>(p.bias) + nh) +
-                                                g);
-                        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const unsigned short lo = static_cast<unsigned short>(w[h] & 0xFFFFu);
-                            const unsigned short hi = static_cast<unsigned short>(w[h] >> 16);
-                            if (p.is_bf16) {
-                                bv[2 * h] = __bfloat162float(__ushort_as_bfloat16(lo));
-                                bv[2 * h + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
-                            } else {
-                                bv[2 * h] = __half2float(__ushort_as_half(lo));
-                                bv[2 * h + 1] = __half2float(__ushort_as_half(hi));
-                            }
+                    for (int h = 0; h < 4; ++h) {
+                        const unsigned short lo = static_cast<unsigned short>(w[h] & 0xFFFFu);
+                        const unsigned short hi = static_cast<unsigned short>(w[h] >> 16);
+                        if (p.is_bf16) {
+                            bv[2 * h] = __bfloat162float(__ushort_as_bfloat16(lo));
+                            bv[2 * h + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
+                        } else {
+                            bv[2 * h] = __half2float(__ushort_as_half(lo));
+                            bv[2 * h + 1] = __half2float(__ushort_as_half(hi));
                         }
-                    } else if (p.has_bias) {
-#pragma unroll
-                        for (int h = 0; h < 8; ++h) {
-                            const int col = nh + g * 8 + h;
-                            bv[h] = (col < p.N) ? bias_val(p.bias, col, p.is_bf16) : 0.0f;
-                        }
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < 8; ++h) bv[h] = 0.0f;
                     }
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
@@ -434,6 +489,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if constexpr (H != SUBS - 1) return;
+                if (p.direct_store && n0 + CW <= p.N) {
+                    // Row `lane` of the chunk: CW * 2 contiguous bytes, 16-byte aligned.
+                    const int row = m0 + lane;
+                    if (row < p.M) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned short *>(p.C) +
+                                                               static_cast<long long>(row) * p.ldc + n0);
+#pragma unroll
+                        for (int j = 0; j < CW / 8; ++j)
+                            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+                    }
+                    return;
+                }
                 // Stage the 32 x CW block: row `lane`, swizzled 16-byte chunks.
                 const uint32_t sb = cstage0 + buf * L::kCStageBytes;
                 uint8_t *sb_gen = cstage_gen0 + buf * L::kCStageBytes;
@@ -510,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++sub;
                 }
             }
+            if (warp == 2 && lane == 0 && tile_i < 8) TGEMM_STAMP(11 + 4 * tile_i);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if (p.tma_store && lane == 0) bulk_wait_group_all();
@@ -519,10 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) TGEMM_STAMP(2);
     if constexpr (CG == 2) cluster_sync();       // both CTAs are done with TMEM and remote barriers
     tc_fence_after();
     if (warp == 1) tmem_dealloc<CG>(tmem_base, L::kTmemCols);
     if constexpr (CG == 2) cluster_sync();       // the peer stays resident until both have freed TMEM
+    if (threadIdx.x == 0) TGEMM_STAMP(3);
 }
 
 }  // namespace tgemm

@@ -41,6 +41,10 @@ struct DeviceInfo {
 
 DeviceInfo g_dev[kMaxDevices];
 
+#ifdef TGEMM_TRACE
+unsigned long long *g_trace_buffer = nullptr;
+#endif
+
 bool device_info(int dev, DeviceInfo **out) {
     if (dev < 0 || dev >= kMaxDevices) return false;
     DeviceInfo &d = g_dev[dev];
@@ -201,7 +205,7 @@ struct Cfg {
     int stages;
     int cg;
     int bit;
-    int cw() const { return (bn % 64 == 0) ? 64 : 32; }   // epilogue chunk / C box width
+    int cw() const { return (bn % 64 == 0) ? 64 : 32; }   // epilogue chunk / C box width (the kernel's kCW)
 };
 constexpr Cfg kCfg256 = {256, 4, 1, 1};
 constexpr Cfg kCfg192 = {192, 4, 1, 32};
@@ -438,6 +442,10 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
+    if (const char *v = std::getenv("TGEMM_STORE")) p.direct_store = (std::atoi(v) == 1 && ldc % 8 == 0) ? 1 : 0;
+#ifdef TGEMM_TRACE
+    p.trace = g_trace_buffer;
+#endif
     const cudaError_t e = launch_config(d, cfg, tma, tmb, tmc, p, stream, bf16);
     release();
     if (e != cudaSuccess) {
@@ -800,3 +808,8 @@ extern "C" tgemm_status tgemm_last_device_status(void) {
 }
 
 extern "C" int tgemm_version(void) { return kVersion; }
+
+#ifdef TGEMM_TRACE
+// Trace builds only: the device buffer the kernels stamp into (8 CTAs x 64).
+extern "C" void tgemm_trace_set_buffer(unsigned long long *dev_ptr) { g_trace_buffer = dev_ptr; }
+#endif
