@@ -75,7 +75,14 @@ struct KParams {
     void *C;                   // used by the masked-store path only
     long long ldc;
     int has_bias, act, is_bf16, tma_store;   // act: 0 none, 1 ReLU, 2 GELU
-    int direct_store;          // 1: full chunks go straight from registers to C (16-byte rows)
+    // Split-K: each tile's k-blocks are cut into split_k ranges of kb_per_split;
+    // unit u = tile * split_k + range.  Every epilogue warp writes its fp32
+    // partial region to `partials`, and the last of the split_k warps covering
+    // that region (counted in `counters`, zero on entry, reset on exit) sums the
+    // partials in range order and runs the epilogue on the complete sum.
+    int split_k, kb_per_split, num_units;
+    float *partials;
+    unsigned int *counters;
     int a_mn;                  // A stored transposed ([K, M], M contiguous): MN-major operand
     int b_kmajor;              // B stored transposed ([N, K], K contiguous): K-major operand
     uint32_t stage_tx;         // bytes one CTA loads per ring stage (depends on the layouts)
@@ -282,12 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t uses[STAGES];
             for (int s = 0; s < STAGES; ++s) uses[s] = 0;
             bool ok = true;
-            for (int t = group_id; t < p.num_tiles && ok; t += num_groups) {
+            for (int u = group_id; u < p.num_units && ok; u += num_groups) {
+                const int t = u / p.split_k;
+                const int kb0 = (u - t * p.split_k) * p.kb_per_split;
+                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
                 int m_blk, n_blk;
                 tile_coords(t, p, m_blk, n_blk);
                 const int a_row = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM;
                 const int b_col = n_blk * BN + static_cast<int>(rank) * L::kBCols;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     const uint32_t a_dst = sbase + L::kOffA + stage * L::kABytes;
                     const uint32_t b_dst = sbase + L::kOffB + stage * L::kBBytes;
@@ -344,14 +354,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             int tile_i = 0;
-            for (int t = group_id; t < p.num_tiles && ok; t += num_groups, ++tile_i) {
+            for (int u = group_id; u < p.num_units && ok; u += num_groups, ++tile_i) {
+                const int t = u / p.split_k;
+                const int kb0 = (u - t * p.split_k) * p.kb_per_split;
+                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
                 if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * L::kAccStride;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_bar(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
                     tc_fence_after();
-                    if (kb == 0 && tile_i < 8) TGEMM_STAMP(8 + 4 * tile_i);
+                    if (kb == kb0 && tile_i < 8) TGEMM_STAMP(8 + 4 * tile_i);
                     const uint32_t a_addr = sbase + L::kOffA + stage * L::kABytes;
                     const uint32_t b_addr = sbase + L::kOffB + stage * L::kBBytes;
 #pragma unroll
@@ -364,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                       : sw128_desc(a_addr + k * (kUmmaK * 2), 16, 1024);
                         const uint64_t bdesc = p.b_kmajor ? sw128_desc(b_addr + k * (kUmmaK * 2), 16, 1024)
                                                           : sw128_desc(b_addr + k * (kUmmaK * 128), kBK * 128, 1024);
-                        mma_f16_ss<CG>(d_tmem, adesc, bdesc, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_ss<CG>(d_tmem, adesc, bdesc, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit<CG>(empty_bar(stage));      // frees the ring stage once read
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -409,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    : static_cast<unsigned short>(0);   // +0.0 in fp16 and bf16
             }
         };
-        if (group_id < p.num_tiles) fetch_bias(group_id);
+        if (group_id < p.num_units) fetch_bias(group_id / p.split_k);
         // Staging swizzle, matching the C tensor map: 16-byte chunk j of row r
         // sits at j ^ (r % 8) for 128-byte rows and j ^ ((r / 2) % 4) for 64-byte rows.
         auto swz = [](int row) { return (CW == 64) ? (row & 7) : ((row >> 1) & 3); };
@@ -422,7 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         int tile_i = 0;
-        for (int t = group_id; t < p.num_tiles; t += num_groups, ++tile_i) {
+        for (int u = group_id; u < p.num_units; u += num_groups, ++tile_i) {
+            const int t = u / p.split_k;
+            const int split = u - t * p.split_k;
             int m_blk, n_blk;
             tile_coords(t, p, m_blk, n_blk);
             int ok = 1;
@@ -437,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kBiasPerLane; ++k)
                 if (lane + 32 * k < static_cast<int>(L::kBiasCols)) bias_s[lane + 32 * k] = bias_next[k];
             __syncwarp();
-            if (t + num_groups < p.num_tiles) fetch_bias(t + num_groups);
+            if (u + num_groups < p.num_units) fetch_bias((u + num_groups) / p.split_k);
             const int m0 = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM + q * 32;
             const int n_tile = n_blk * BN;
             // Only chunks / rows that intersect C are read out and stored (no
@@ -489,18 +504,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if constexpr (H != SUBS - 1) return;
-                if (p.direct_store && n0 + CW <= p.N) {
-                    // Row `lane` of the chunk: CW * 2 contiguous bytes, 16-byte aligned.
-                    const int row = m0 + lane;
-                    if (row < p.M) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned short *>(p.C) +
-                                                               static_cast<long long>(row) * p.ldc + n0);
-#pragma unroll
-                        for (int j = 0; j < CW / 8; ++j)
-                            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
-                    }
-                    return;
-                }
                 // Stage the 32 x CW block: row `lane`, swizzled 16-byte chunks.
                 const uint32_t sb = cstage0 + buf * L::kCStageBytes;
                 uint8_t *sb_gen = cstage_gen0 + buf * L::kCStageBytes;
@@ -548,7 +551,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if constexpr (L::kCBufs == 2) buf ^= 1;
             };
-            if (n_sub == 0) {
+            // Dispatches sub-chunk `sub` to the right half (compile-time index).
+            auto process_sub = [&](int sub, const uint32_t (&r)[32]) {
+                if (sub % SUBS == SUBS - 1) process(std::integral_constant<int, SUBS - 1>{}, sub, r);
+                else process(std::integral_constant<int, 0>{}, sub, r);
+            };
+            // Split-K: this warp's fp32 partial region of unit (t, range); float4 g
+            // of lane l's 32 values of sub-chunk `sub` sits at sub*1024 + g*128 + l*4.
+            constexpr int kMaxSub = L::kBiasCols / 32;
+            // Regions and counters are per (tile, range, CTA of the group, epilogue warp).
+            const int wid = static_cast<int>(rank) * kEpiWarps + ew;
+            auto region = [&](int range) {
+                return p.partials + ((static_cast<long long>(t) * p.split_k + range) * (CG * kEpiWarps) + wid) *
+                                        (kMaxSub * 1024);
+            };
+            if (p.split_k > 1) {
+                if (n_sub == 0) {
+                    release_acc(acc);
+                } else {
+                    float *mine = region(split);
+                    uint32_t ra[32];
+#pragma unroll 1
+                    for (int sub = 0; sub < n_sub; ++sub) {
+                        tload(sub, ra);
+                        tmem_wait_ld();
+                        if (sub == n_sub - 1) release_acc(acc);
+#pragma unroll
+                        for (int g = 0; g < 8; ++g)
+                            __stcg(reinterpret_cast<float4 *>(mine + sub * 1024 + g * 128 + lane * 4),
+                                   make_float4(__uint_as_float(ra[4 * g]), __uint_as_float(ra[4 * g + 1]),
+                                               __uint_as_float(ra[4 * g + 2]), __uint_as_float(ra[4 * g + 3])));
+                    }
+                    __threadfence();
+                    __syncwarp();
+                    unsigned int arrived = 0;
+                    if (lane == 0) arrived = atomicAdd(p.counters + t * (CG * kEpiWarps) + wid, 1u);
+                    arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                    if (arrived == static_cast<unsigned int>(p.split_k - 1)) {
+                        // Last of the ranges for this region: sum all partials in range
+                        // order (the same order every run), then the normal epilogue.
+                        __threadfence();
+#pragma unroll 1
+                        for (int sub = 0; sub < n_sub; ++sub) {
+                            float acc_v[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) acc_v[j] = 0.0f;
+#pragma unroll 1
+                            for (int rg = 0; rg < p.split_k; ++rg) {
+                                const float *src = region(rg) + sub * 1024 + lane * 4;
+#pragma unroll
+                                for (int g = 0; g < 8; ++g) {
+                                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + g * 128));
+                                    acc_v[4 * g] += v.x;
+                                    acc_v[4 * g + 1] += v.y;
+                                    acc_v[4 * g + 2] += v.z;
+                                    acc_v[4 * g + 3] += v.w;
+                                }
+                            }
+                            uint32_t rs[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) rs[j] = __float_as_uint(acc_v[j]);
+                            process_sub(sub, rs);
+                        }
+                        __syncwarp();
+                        if (lane == 0) p.counters[t * (CG * kEpiWarps) + wid] = 0u;   // ready for the next launch
+                    }
+                }
+            } else if (n_sub == 0) {
                 release_acc(acc);
             } else {
                 // The next sub-chunk's TMEM load is in flight while one is processed;

@@ -322,21 +322,26 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
     p.num_n = static_cast<int>(cdiv(p.N, cfg.bn));
     p.num_kb = static_cast<int>(cdiv(p.K, kBK));
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
-    if (tiles > INT32_MAX) return cudaErrorInvalidValue;
+    if (p.split_k < 1) p.split_k = 1;
+    p.kb_per_split = static_cast<int>(cdiv(p.num_kb, p.split_k));
+    p.split_k = static_cast<int>(cdiv(p.num_kb, p.kb_per_split));   // no empty k ranges
+    const int64_t units = tiles * p.split_k;
+    if (units > INT32_MAX) return cudaErrorInvalidValue;
     p.num_tiles = static_cast<int>(tiles);
+    p.num_units = static_cast<int>(units);
     int group_m = 16;
     if (const char *g = std::getenv("TGEMM_GROUP_M")) group_m = std::max(1, std::atoi(g));
     p.group_m = std::min(p.num_m, group_m);
     p.idesc = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(cfg.bn),
                         p.a_mn != 0, p.b_kmajor == 0);
     switch (cfg.bit) {
-        case 1: return launch_fused<256, 4, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
-        case 2: return launch_fused<128, 6, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
-        case 4: return launch_fused<64, 8, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
-        case 8: return launch_fused<256, 6, 2>(d, cfg.bit, ta, tb, tc, p, tiles, s);
-        case 16: return launch_fused<128, 8, 2>(d, cfg.bit, ta, tb, tc, p, tiles, s);
-        case 32: return launch_fused<192, 4, 1>(d, cfg.bit, ta, tb, tc, p, tiles, s);
-        default: return launch_fused<224, 6, 2>(d, cfg.bit, ta, tb, tc, p, tiles, s);
+        case 1: return launch_fused<256, 4, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 2: return launch_fused<128, 6, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 4: return launch_fused<64, 8, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 8: return launch_fused<256, 6, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 16: return launch_fused<128, 8, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 32: return launch_fused<192, 4, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
+        default: return launch_fused<224, 6, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
     }
 }
 
@@ -371,6 +376,25 @@ bool encode_maps(const Cfg &cfg, const void *a, int64_t lda, int ta, const void 
     return ok;
 }
 
+// Split-K for problems whose tiles cannot fill the GPU (small M, the decode
+// shapes): ranges of k per tile so that tiles x ranges about fills the SMs (or
+// SM pairs), each range at least 4 k-blocks, at most 16 ranges.
+int choose_split(const Cfg &cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (const char *f = std::getenv("TGEMM_SPLIT_K")) return std::max(1, std::atoi(f));
+    const int64_t groups = cfg.cg == 2 ? num_sms / 2 : num_sms;
+    const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn);
+    const int64_t kb = cdiv(K, kBK);
+    if (tiles * 2 > groups || kb < 8) return 1;
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({groups / tiles, kb / 4, 16})));
+}
+
+// fp32 partial floats per (tile, range): one region per epilogue warp of each CTA.
+int64_t partial_floats_per_unit(const Cfg &cfg) {
+    const int cw = cfg.cw();
+    const int64_t max_sub = ((cfg.bn / cw + 1) / 2) * cw / 32;
+    return static_cast<int64_t>(cfg.cg) * kEpiWarps * max_sub * 1024;
+}
+
 tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void *bias, void *C,
                         int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                         int dtype, int epilogue, cudaStream_t stream, int ta = 0, int tb = 0) {
@@ -393,9 +417,11 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     const void *a_use = A, *b_use = B;
     int64_t lda_use = lda, ldb_use = ldb;
     tgemm_status st = TGEMM_OK;
+    void *scratch_split = nullptr;
     auto release = [&]() {
         if (scratch_a) cudaFreeAsync(scratch_a, stream);
         if (scratch_b) cudaFreeAsync(scratch_b, stream);
+        if (scratch_split) cudaFreeAsync(scratch_split, stream);
     };
     const int64_t a_rows = ta ? K : M, a_cols = ta ? M : K;
     const int64_t b_rows = tb ? N : K, b_cols = tb ? K : N;
@@ -442,10 +468,26 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
-    if (const char *v = std::getenv("TGEMM_STORE")) p.direct_store = (std::atoi(v) == 1 && ldc % 8 == 0) ? 1 : 0;
 #ifdef TGEMM_TRACE
     p.trace = g_trace_buffer;
 #endif
+    // Split-K scratch: the fp32 partials and one zeroed counter per (tile, epilogue warp).
+    p.split_k = choose_split(cfg, M, N, K, d->num_sms);
+    if (p.split_k > 1) {
+        const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn);
+        const int64_t pbytes = tiles * p.split_k * partial_floats_per_unit(cfg) * 4;
+        const int64_t cbytes = tiles * cfg.cg * kEpiWarps * 4;
+        if (cudaMallocFromPoolAsync(&scratch_split, static_cast<size_t>(pbytes + cbytes), d->pool, stream) !=
+                cudaSuccess ||
+            cudaMemsetAsync(static_cast<char *>(scratch_split) + pbytes, 0, static_cast<size_t>(cbytes), stream) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            release();
+            return TGEMM_ERR_CUDA;
+        }
+        p.partials = static_cast<float *>(scratch_split);
+        p.counters = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch_split) + pbytes);
+    }
     const cudaError_t e = launch_config(d, cfg, tma, tmb, tmc, p, stream, bf16);
     release();
     if (e != cudaSuccess) {

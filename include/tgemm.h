@@ -91,6 +91,12 @@ typedef enum {
  * returned to it on `stream`; when ldc is not a multiple of 8 the epilogue
  * stores C with plain masked stores instead of tensor-memory-access stores.
  *
+ * Problems with too few output tiles to fill the GPU (few rows, e.g. decode
+ * shapes) split the k loop of each tile across CTAs: fp32 partial sums go to
+ * pool scratch and the last CTA to finish a tile region adds them in a fixed
+ * order before the epilogue, so results are deterministic; they may differ
+ * in the last bits from an unsplit run (different summation order).
+ *
  * Asynchrony: returns once the work is enqueued; the caller synchronises.
  * Thread safety: safe to call from several host threads.
  */

@@ -145,6 +145,32 @@ def test_pair_rows_beyond_m(cuda_lib, monkeypatch, cfg):
         assert_bit_exact(got, oracle_ref(inputs, M, N, K, "fp16", "bias_relu"), "fp16", f"{cfg} {M}x{N}x{K}")
 
 
+# ------------------------------------------------------------------ split-K
+@pytest.mark.parametrize("cfg", CONFIGS)
+@pytest.mark.parametrize("split", ["2", "3", "5"])
+def test_split_k_forced(cuda_lib, monkeypatch, cfg, split):
+    """k ranges of a tile computed by different CTAs, fp32 partials summed by the
+    last arriving warp of each region, then the epilogue (bit-exact on integers)."""
+    monkeypatch.setenv("TGEMM_FORCE_CFG", cfg)
+    monkeypatch.setenv("TGEMM_SPLIT_K", split)
+    M, N, K = 333, 700, 1000
+    inputs, got = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=41, kind="int")
+    assert_bit_exact(got, oracle_ref(inputs, M, N, K, "fp16", "bias_relu"), "fp16", f"{cfg} split={split}")
+    inputs, got = run_tgemm(cuda_lib, M, N, K, "bf16", "bias_gelu", seed=42, kind="gelu")
+    check_epilogue(got, inputs, M, N, K, "bf16", "bias_gelu", f"{cfg} split={split}")
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 128])
+def test_decode_shapes_split_automatically(cuda_lib, M):
+    """Few-row (decode-like) shapes: too few tiles for the GPU, so the k loop is
+    split; the result must not depend on the split (deterministic order)."""
+    N, K = 4096, 8192
+    inputs, got = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=43 + M)
+    check_epilogue(got, inputs, M, N, K, "fp16", "bias_relu", f"M={M}")
+    _, again = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=43 + M)
+    assert np.array_equal(got, again)
+
+
 # ------------------------------------------------------------------ layouts
 @pytest.mark.parametrize("ta,tb", [(0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("cfg", CONFIGS)
