@@ -19,7 +19,9 @@ STATUS = {0: "TGEMM_OK", 1: "TGEMM_ERR_INVALID_ARG", 2: "TGEMM_ERR_ALIGNMENT",
           3: "TGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TGEMM_ERR_ALIAS", 5: "TGEMM_ERR_CUDA",
           6: "TGEMM_ERR_TIMEOUT", 7: "TGEMM_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("tgemm_run", "tgemm_run_ex", "tgemm_run_host", "tgemm_status_string",
-            "tgemm_last_device_status", "tgemm_version", "tgemm_run_noalloc")
+            "tgemm_last_device_status", "tgemm_version", "tgemm_run_noalloc", "tgemm_plan")
+PLAN_FIELDS = ("bn", "cg", "stages", "tiles", "groups", "split_k", "split_first", "narrow_first",
+               "narrow_parts", "units")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lock = threading.Lock()
@@ -60,6 +62,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.tgemm_last_device_status.restype = i32
         lib.tgemm_version.argtypes = []
         lib.tgemm_version.restype = i32
+        lib.tgemm_plan.argtypes = [i64, i64, i64, i32, p]
+        lib.tgemm_plan.restype = i32
         _lib = lib
         return lib
 
@@ -108,3 +112,12 @@ def tgemm_last_device_status() -> int:
 
 def tgemm_version() -> int:
     return int(load().tgemm_version())
+
+
+def tgemm_plan(M: int, N: int, K: int, num_sms: int) -> dict:
+    """The work plan of an M x N x K problem on `num_sms` SMs (host logic, no GPU)."""
+    out = (ctypes.c_int32 * len(PLAN_FIELDS))()
+    st = load().tgemm_plan(M, N, K, num_sms, ctypes.cast(out, ctypes.c_void_p))
+    if st != 0:
+        raise TgemmError(st, "tgemm_plan")
+    return dict(zip(PLAN_FIELDS, (int(v) for v in out)))

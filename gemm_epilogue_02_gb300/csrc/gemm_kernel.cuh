@@ -75,12 +75,22 @@ struct KParams {
     void *C;                   // used by the masked-store path only
     long long ldc;
     int has_bias, act, is_bf16, tma_store;   // act: 0 none, 1 ReLU, 2 GELU
-    // Split-K: each tile's k-blocks are cut into split_k ranges of kb_per_split;
-    // unit u = tile * split_k + range.  Every epilogue warp writes its fp32
+    // Split-K: the tiles from split_first on (the remainder that does not fill
+    // a whole wave, or all tiles of a small problem) have their k-blocks cut
+    // into split_k ranges of kb_per_split.  Units 0 .. num_split_units-1 are
+    // those (tile, range) pieces and come first; the remaining units are whole
+    // tiles 0 .. split_first-1.  Every epilogue warp of a piece writes its fp32
     // partial region to `partials`, and the last of the split_k warps covering
     // that region (counted in `counters`, zero on entry, reset on exit) sums the
     // partials in range order and runs the epilogue on the complete sum.
-    int split_k, kb_per_split, num_units;
+    int split_k, kb_per_split, split_first, num_split_units, num_units;
+    // Narrow tail: tiles narrow_first .. split_first-1 (the last, partial wave)
+    // are each cut into narrow_parts column parts of BN / narrow_parts columns;
+    // those units come last and use their own MMA width (idesc_narrow) and
+    // per-stage byte count (stage_tx_narrow).  No reduction is needed: every
+    // output element is still one whole k loop.
+    int narrow_first, narrow_parts;
+    uint32_t stage_tx_narrow, idesc_narrow;
     float *partials;
     unsigned int *counters;
     int a_mn;                  // A stored transposed ([K, M], M contiguous): MN-major operand
@@ -93,18 +103,33 @@ struct KParams {
 #endif
 };
 
-// Trace builds only (-DTGEMM_TRACE): %globaltimer stamps of CTAs 0..7 into
+// Trace builds only (-DTGEMM_TRACE): %globaltimer stamps of CTAs 0..159 into
 // p.trace[cta * 64 + slot].  Slots: 0 entry, 1 set-up done, 2 teardown start,
-// 3 exit; per tile i < 8: 8+4i first MMA issued, 9+4i last MMA committed,
-// 10+4i epilogue start (warp 2), 11+4i epilogue stores issued (warp 2).
+// 3 exit, 4 shared-memory base, 5 / 6 SM clock at entry / exit; per unit
+// i < 8: 8+4i first MMA issued, 9+4i last MMA committed, 10+4i epilogue start
+// (warp 2), 11+4i epilogue stores issued (warp 2); first unit split in k:
+// 40 partials written, 41 fence done, 42 counter taken, 43 arrival index + 1,
+// 44 reduction done (last arriver only).  The buffer holds 10240 + 384 words.
 #ifdef TGEMM_TRACE
 #define TGEMM_STAMP(slot)                                                                         \
     do {                                                                                          \
-        if (blockIdx.x < 8 && (slot) < 64) p.trace[blockIdx.x * 64 + (slot)] = globaltimer_ns(); \
+        if (blockIdx.x < 160 && (slot) < 64) p.trace[blockIdx.x * 64 + (slot)] = globaltimer_ns(); \
+    } while (0)
+// Stage timeline (SM clock cycles) of CTA 0 for the second unit's first 64
+// k-blocks: p.trace[10240 + kind * 64 + i], kind 0 producer before the empty
+// wait, 1 producer past it, 2 producer loads issued, 3 MMA before the full
+// wait, 4 MMA past it, 5 MMA commit issued.
+#define TGEMM_STAGE_STAMP(kind, i)                                                           \
+    do {                                                                                     \
+        if (blockIdx.x == 0 && (i) >= 0 && (i) < 64)                                         \
+            p.trace[10240 + (kind) * 64 + (i)] = clock64();                                  \
     } while (0)
 #else
 #define TGEMM_STAMP(slot) \
     do {                  \
+    } while (0)
+#define TGEMM_STAGE_STAMP(kind, i) \
+    do {                           \
     } while (0)
 #endif
 
@@ -147,13 +172,19 @@ struct Smem {
 };
 
 // Bounded wait.  Returns false if the CTA is aborting or the limit ran out.
+// The MMA lane's wait for operands spins (its data is normally there already);
+// every other wait sleeps in try_wait, because a spinning lane takes issue
+// slots from the warps that share its scheduler, the MMA lane among them.
+template <bool kSleep>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                          unsigned int *status) {
-    if (mbar_try_wait(bar, parity)) return true;
+    constexpr uint32_t kHintNs = 20000;
+    auto test = [&]() { return kSleep ? mbar_try_wait_sleep(bar, parity, kHintNs) : mbar_try_wait(bar, parity); };
+    if (test()) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 127u) == 0) {
+        if (test()) return true;
+        if (kSleep || (it & 127u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 *abort_flag = 1;
@@ -180,6 +211,42 @@ __device__ __forceinline__ void tile_coords(int t, const KParams &p, int &m_blk,
     const int local = t - g * per_group;
     m_blk = first_m + local % gsize;
     n_blk = local / gsize;
+}
+
+// A work unit: tile t, its k-block range [kb0, kb1) (range index, -1 for the
+// whole k loop) and its columns [col0, col0 + width) within the tile.
+struct Unit {
+    int t, kb0, kb1, range, col0, width;
+};
+
+// Unit order: split-K pieces, then whole tiles 0 .. narrow_first-1, then the
+// column parts of the narrow tiles.
+__device__ __forceinline__ Unit unit_info(int u, const KParams &p, int bn) {
+    Unit w;
+    w.kb0 = 0;
+    w.kb1 = p.num_kb;
+    w.range = -1;
+    w.col0 = 0;
+    w.width = bn;
+    if (u < p.num_split_units) {
+        const int i = u / p.split_k;
+        w.t = p.split_first + i;
+        w.range = u - i * p.split_k;
+        w.kb0 = w.range * p.kb_per_split;
+        w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
+        return w;
+    }
+    const int v = u - p.num_split_units;
+    if (v < p.narrow_first) {
+        w.t = v;
+        return w;
+    }
+    const int x = v - p.narrow_first;
+    const int i = x / p.narrow_parts;
+    w.t = p.narrow_first + i;
+    w.width = bn / p.narrow_parts;
+    w.col0 = (x - i * p.narrow_parts) * w.width;
+    return w;
 }
 
 __device__ __forceinline__ float bias_val(const void *bias, int idx, int is_bf16) {
@@ -242,7 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) TGEMM_STAMP(0);
 #ifdef TGEMM_TRACE
-    if (threadIdx.x == 0 && blockIdx.x < 8) p.trace[blockIdx.x * 64 + 4] = smem_u32(smem_raw);
+    if (threadIdx.x == 0 && blockIdx.x < 160) {
+        p.trace[blockIdx.x * 64 + 4] = smem_u32(smem_raw);
+        p.trace[blockIdx.x * 64 + 5] = clock64();
+    }
 #endif
     const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
     const int group_id = (CG == 2) ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
@@ -290,22 +360,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < STAGES; ++s) uses[s] = 0;
             bool ok = true;
             for (int u = group_id; u < p.num_units && ok; u += num_groups) {
-                const int t = u / p.split_k;
-                const int kb0 = (u - t * p.split_k) * p.kb_per_split;
-                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+                const Unit w = unit_info(u, p, BN);
                 int m_blk, n_blk;
-                tile_coords(t, p, m_blk, n_blk);
+                tile_coords(w.t, p, m_blk, n_blk);
+                const bool narrow = w.width != BN;
                 const int a_row = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM;
-                const int b_col = n_blk * BN + static_cast<int>(rank) * L::kBCols;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                // Each CTA of the group holds width / CG columns of the unit's B.
+                const int b_col = n_blk * BN + w.col0 + static_cast<int>(rank) * (w.width / CG);
+                const int b_sub = narrow ? (w.width / CG) / 64 : L::kBSub;
+                const uint32_t tx = narrow ? p.stage_tx_narrow : p.stage_tx;
+                const bool st_trace = (u == group_id + num_groups);
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                    if (st_trace) TGEMM_STAGE_STAMP(0, kb - w.kb0);
+                    if (!wait_bar<true>(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    if (st_trace) TGEMM_STAGE_STAMP(1, kb - w.kb0);
                     const uint32_t a_dst = sbase + L::kOffA + stage * L::kABytes;
                     const uint32_t b_dst = sbase + L::kOffB + stage * L::kBBytes;
                     // Rank 0 announces the bytes of the whole group; with a CTA pair the
                     // peer's copies report to rank 0's barrier (its transaction count may
                     // dip below zero until the announcement lands, which is allowed).
                     const uint32_t fb = (CG == 1) ? full_bar(stage) : leader_full(stage);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), CG * p.stage_tx);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), CG * tx);
                     auto load = [&](uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y) {
                         if constexpr (CG == 1) tma_load_2d(dst, m, fb, x, y);
                         else tma_load_2d_pair(dst, m, fb, x, y);
@@ -323,11 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // B [K, N]: 64-column sub-tiles of 64 k-rows (MN-major).
 #pragma unroll
                         for (int j = 0; j < L::kBSub; ++j)
-                            load(b_dst + j * (kBK * 128), &tmB, b_col + j * 64, kb * kBK);
+                            if (j < b_sub) load(b_dst + j * (kBK * 128), &tmB, b_col + j * 64, kb * kBK);
                     } else {
-                        // B stored [N, K]: one box of BN/CG n-rows x 64 k (K-major).
+                        // B stored [N, K]: one box of BN/CG n-rows x 64 k (K-major); a
+                        // narrow unit's MMA reads only the first width / CG of them.
                         load(b_dst, &tmB, kb * kBK, b_col);
                     }
+                    if (st_trace) TGEMM_STAGE_STAMP(2, kb - w.kb0);
                     ++uses[stage];
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -354,32 +431,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             int tile_i = 0;
+            // Shared-memory descriptors of ring stage 0 and their steps, in the
+            // descriptor's 16-byte address units, so that the loop only adds.
+            // K-major operand: 8-row groups 1 KiB apart (stride); a 16-wide k step
+            // is 32 B along the 128-byte row.  MN-major operand: 64-element
+            // sub-tiles kBK*128 B apart (leading), 8-row k groups 1 KiB apart
+            // (stride); a 16-wide k step is 16 rows = 2 KiB.
+            const uint64_t a_desc0 = p.a_mn ? sw128_desc(sbase + L::kOffA, kBK * 128, 1024)
+                                            : sw128_desc(sbase + L::kOffA, 16, 1024);
+            const uint64_t b_desc0 = p.b_kmajor ? sw128_desc(sbase + L::kOffB, 16, 1024)
+                                                : sw128_desc(sbase + L::kOffB, kBK * 128, 1024);
+            const uint32_t a_kstep = p.a_mn ? (kUmmaK * 128) >> 4 : (kUmmaK * 2) >> 4;
+            const uint32_t b_kstep = p.b_kmajor ? (kUmmaK * 2) >> 4 : (kUmmaK * 128) >> 4;
             for (int u = group_id; u < p.num_units && ok; u += num_groups, ++tile_i) {
-                const int t = u / p.split_k;
-                const int kb0 = (u - t * p.split_k) * p.kb_per_split;
-                const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
-                if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                const Unit w = unit_info(u, p, BN);
+                const int kb0 = w.kb0, kb1 = w.kb1;
+                const uint32_t idesc = (w.width != BN) ? p.idesc_narrow : p.idesc;
+                if (!wait_bar<true>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * L::kAccStride;
+                uint32_t accumulate = 0u;   // the unit's first MMA overwrites the accumulator
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_bar(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                    if (tile_i == 1) TGEMM_STAGE_STAMP(3, kb - kb0);
+                    if (!wait_bar<false>(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                    if (tile_i == 1) TGEMM_STAGE_STAMP(4, kb - kb0);
                     tc_fence_after();
                     if (kb == kb0 && tile_i < 8) TGEMM_STAMP(8 + 4 * tile_i);
-                    const uint32_t a_addr = sbase + L::kOffA + stage * L::kABytes;
-                    const uint32_t b_addr = sbase + L::kOffB + stage * L::kBBytes;
+                    const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (L::kABytes >> 4);
+                    const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (L::kBBytes >> 4);
+                    mma_f16_ss<CG>(d_tmem, ad, bd, idesc, accumulate);
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        // K-major operand: 8-row groups 1 KiB apart (stride); a 16-wide k step
-                        // is 32 B along the 128-byte row.  MN-major operand: 64-element
-                        // sub-tiles kBK*128 B apart (leading), 8-row k groups 1 KiB apart
-                        // (stride); a 16-wide k step is 16 rows = 2 KiB.
-                        const uint64_t adesc = p.a_mn ? sw128_desc(a_addr + k * (kUmmaK * 128), kBK * 128, 1024)
-                                                      : sw128_desc(a_addr + k * (kUmmaK * 2), 16, 1024);
-                        const uint64_t bdesc = p.b_kmajor ? sw128_desc(b_addr + k * (kUmmaK * 2), 16, 1024)
-                                                          : sw128_desc(b_addr + k * (kUmmaK * 128), kBK * 128, 1024);
-                        mma_f16_ss<CG>(d_tmem, adesc, bdesc, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-                    }
+                    for (int k = 1; k < kBK / kUmmaK; ++k)
+                        mma_f16_ss<CG>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
+                    accumulate = 1u;
                     mma_commit<CG>(empty_bar(stage));      // frees the ring stage once read
+                    if (tile_i == 1) TGEMM_STAGE_STAMP(5, kb - kb0);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
@@ -408,21 +494,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned short *bias_s = reinterpret_cast<unsigned short *>(smem + L::kOffBias) + ew * L::kBiasCols;
         constexpr int kBiasPerLane = (L::kBiasCols + 31) / 32;
         unsigned short bias_next[kBiasPerLane];
-        // Loads (into registers) the bias columns this warp needs for tile t.
-        auto fetch_bias = [&](int t) {
+        // Loads (into registers) the bias columns this warp needs for unit u.
+        auto fetch_bias = [&](int u) {
+            const Unit w = unit_info(u, p, BN);
             int mb, nb;
-            tile_coords(t, p, mb, nb);
+            tile_coords(w.t, p, mb, nb);
 #pragma unroll
             for (int k = 0; k < kBiasPerLane; ++k) {
                 const int i = lane + 32 * k;
-                const int col = nb * BN + (part + 2 * (i / CW)) * CW + i % CW;
+                const int col = nb * BN + w.col0 + (part + 2 * (i / CW)) * CW + i % CW;
                 bias_next[k] = (p.has_bias && i < static_cast<int>(L::kBiasCols) && col < p.N &&
-                                (part + 2 * (i / CW)) * CW < BN)
+                                (part + 2 * (i / CW)) * CW < w.width)
                                    ? __ldg(reinterpret_cast<const unsigned short *>(p.bias) + col)
                                    : static_cast<unsigned short>(0);   // +0.0 in fp16 and bf16
             }
         };
-        if (group_id < p.num_units) fetch_bias(group_id / p.split_k);
+        if (group_id < p.num_units) fetch_bias(group_id);
         // Staging swizzle, matching the C tensor map: 16-byte chunk j of row r
         // sits at j ^ (r % 8) for 128-byte rows and j ^ ((r / 2) % 4) for 64-byte rows.
         auto swz = [](int row) { return (CW == 64) ? (row & 7) : ((row >> 1) & 3); };
@@ -436,12 +523,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int tile_i = 0;
         for (int u = group_id; u < p.num_units; u += num_groups, ++tile_i) {
-            const int t = u / p.split_k;
-            const int split = u - t * p.split_k;
+            const Unit w = unit_info(u, p, BN);
+            const int t = w.t, split = w.range;
             int m_blk, n_blk;
             tile_coords(t, p, m_blk, n_blk);
             int ok = 1;
-            if (lane == 0) ok = wait_bar(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
+            if (lane == 0) ok = wait_bar<true>(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
@@ -452,12 +539,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kBiasPerLane; ++k)
                 if (lane + 32 * k < static_cast<int>(L::kBiasCols)) bias_s[lane + 32 * k] = bias_next[k];
             __syncwarp();
-            if (u + num_groups < p.num_units) fetch_bias((u + num_groups) / p.split_k);
+            if (u + num_groups < p.num_units) fetch_bias(u + num_groups);
             const int m0 = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM + q * 32;
-            const int n_tile = n_blk * BN;
+            const int n_tile = n_blk * BN + w.col0;     // accumulator column 0 is C column n_tile
             // Only chunks / rows that intersect C are read out and stored (no
             // store is ever issued at a coordinate outside the tensor).
-            const int c_end = (m0 < p.M) ? min(BN / CW, (p.N - n_tile + CW - 1) / CW) : 0;
+            const int c_end = (m0 < p.M && n_tile < p.N) ? min(w.width / CW, (p.N - n_tile + CW - 1) / CW) : 0;
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc) * L::kAccStride;
             // TMEM is read in 32-column sub-chunks; a chunk is CW / 32 of them.
@@ -561,11 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr int kMaxSub = L::kBiasCols / 32;
             // Regions and counters are per (tile, range, CTA of the group, epilogue warp).
             const int wid = static_cast<int>(rank) * kEpiWarps + ew;
+            const int ts = t - p.split_first;     // index among the split tiles
             auto region = [&](int range) {
-                return p.partials + ((static_cast<long long>(t) * p.split_k + range) * (CG * kEpiWarps) + wid) *
+                return p.partials + ((static_cast<long long>(ts) * p.split_k + range) * (CG * kEpiWarps) + wid) *
                                         (kMaxSub * 1024);
             };
-            if (p.split_k > 1) {
+            if (split >= 0) {
                 if (n_sub == 0) {
                     release_acc(acc);
                 } else {
@@ -582,11 +670,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    make_float4(__uint_as_float(ra[4 * g]), __uint_as_float(ra[4 * g + 1]),
                                                __uint_as_float(ra[4 * g + 2]), __uint_as_float(ra[4 * g + 3])));
                     }
+                    if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(40);
                     __threadfence();
                     __syncwarp();
+                    if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(41);
                     unsigned int arrived = 0;
-                    if (lane == 0) arrived = atomicAdd(p.counters + t * (CG * kEpiWarps) + wid, 1u);
+                    if (lane == 0) arrived = atomicAdd(p.counters + ts * (CG * kEpiWarps) + wid, 1u);
                     arrived = __shfl_sync(0xffffffffu, arrived, 0);
+#ifdef TGEMM_TRACE
+                    if (warp == 2 && lane == 0 && tile_i == 0 && blockIdx.x < 160) {
+                        TGEMM_STAMP(42);
+                        p.trace[blockIdx.x * 64 + 43] = arrived + 1;
+                    }
+#endif
                     if (arrived == static_cast<unsigned int>(p.split_k - 1)) {
                         // Last of the ranges for this region: sum all partials in range
                         // order (the same order every run), then the normal epilogue.
@@ -614,7 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             process_sub(sub, rs);
                         }
                         __syncwarp();
-                        if (lane == 0) p.counters[t * (CG * kEpiWarps) + wid] = 0u;   // ready for the next launch
+                        if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(44);
+                        if (lane == 0) p.counters[ts * (CG * kEpiWarps) + wid] = 0u;   // ready for the next launch
                     }
                 }
             } else if (n_sub == 0) {
@@ -662,6 +759,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc<CG>(tmem_base, L::kTmemCols);
     if constexpr (CG == 2) cluster_sync();       // the peer stays resident until both have freed TMEM
     if (threadIdx.x == 0) TGEMM_STAMP(3);
+#ifdef TGEMM_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < 160) p.trace[blockIdx.x * 64 + 6] = clock64();
+#endif
 }
 
 }  // namespace tgemm

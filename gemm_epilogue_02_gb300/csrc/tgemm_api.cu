@@ -217,13 +217,38 @@ constexpr Cfg kCfg128x2 = {128, 8, 2, 16};
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Column parts a tile of `cfg` may be cut into for the narrow tail: each CTA
+// must still load whole 64-column sub-tiles of B.
+int max_narrow_parts(const Cfg &cfg) {
+    int parts = 1;
+    while (parts < 4 && (cfg.bn / cfg.cg / (2 * parts)) % 64 == 0 && cfg.bn / cfg.cg / (2 * parts) >= 64) parts *= 2;
+    return parts;
+}
+
+// Parts each remainder tile is cut into: the largest power of two that the
+// tile allows and that still fits the partial wave's units on `groups`.
+int narrow_parts_for(const Cfg &cfg, int64_t rem, int64_t groups) {
+    int s = 1;
+    while (2 * s <= max_narrow_parts(cfg) && rem * 2 * s <= groups) s *= 2;
+    return s;
+}
+
+// Waves of tiles on `groups` SMs (or SM pairs), counting a last partial wave
+// as the fraction of a tile its narrow parts take.
+double effective_waves(const Cfg &cfg, int64_t tiles, int64_t groups) {
+    const int64_t full = tiles / groups, rem = tiles % groups;
+    if (rem == 0) return static_cast<double>(full);
+    if (full == 0) return 1.0;   // a single partial wave is not cut
+    return static_cast<double>(full) + 1.0 / narrow_parts_for(cfg, rem, groups);
+}
+
 // Tile-shape rule.  Per-SM time of a tile is proportional to its width (the
 // MMA rows per SM are fixed at 128), so the estimated kernel time is
-// waves x width x (relative cost per column: narrow single-CTA tiles re-read A
-// from shared memory more often and run slower per column, measured on the
-// 8192^3 workload).  CTA pairs are preferred whenever their tiles fill every
-// SM pair at least once.
-Cfg choose_config(int64_t M, int64_t N, int num_sms) {
+// effective waves x width x a relative cost per column (narrow single-CTA tiles
+// re-read A from shared memory more often, and a 224-wide pair tile runs at
+// the speed of a 256-wide one; measured on the 8192^3 workload).  CTA pairs
+// are preferred whenever their tiles fill every SM pair at least once.
+Cfg choose_config(int64_t M, int64_t N, int64_t K, int num_sms) {
     if (const char *f = std::getenv("TGEMM_FORCE_CFG")) {
         const std::string v(f);
         if (v == "256") return kCfg256;
@@ -235,15 +260,15 @@ Cfg choose_config(int64_t M, int64_t N, int num_sms) {
         if (v == "128x2") return kCfg128x2;
     }
     struct Cand { Cfg cfg; double per_col; };
+    (void)K;
     const int pairs = num_sms / 2;
     if (M > kBM && cdiv(M, 2 * kBM) * cdiv(N, 256) >= pairs) {
-        const Cand cands[2] = {{kCfg256x2, 1.0}, {kCfg224x2, 1.1}};
+        const Cand cands[2] = {{kCfg256x2, 1.0}, {kCfg224x2, 256.0 / 224.0}};
         Cfg best = kCfg256x2;
         double best_cost = 1e300;
         for (const Cand &c : cands) {
-            const double waves = static_cast<double>(cdiv(cdiv(M, 2 * kBM) * cdiv(N, c.cfg.bn), pairs));
-            const double cost = waves * c.cfg.bn * c.per_col;
-            if (cost < best_cost) { best_cost = cost; best = c.cfg; }
+            const double cost = effective_waves(c.cfg, cdiv(M, 2 * kBM) * cdiv(N, c.cfg.bn), pairs) * c.cfg.bn * c.per_col;
+            if (cost < best_cost - 1e-9) { best_cost = cost; best = c.cfg; }
         }
         return best;
     }
@@ -251,8 +276,7 @@ Cfg choose_config(int64_t M, int64_t N, int num_sms) {
     Cfg best = kCfg256;
     double best_cost = 1e300;
     for (const Cand &c : cands) {
-        const double waves = static_cast<double>(cdiv(cdiv(M, kBM) * cdiv(N, c.cfg.bn), num_sms));
-        const double cost = waves * c.cfg.bn * c.per_col;
+        const double cost = effective_waves(c.cfg, cdiv(M, kBM) * cdiv(N, c.cfg.bn), num_sms) * c.cfg.bn * c.per_col;
         if (cost < best_cost) { best_cost = cost; best = c.cfg; }
     }
     return best;
@@ -294,6 +318,10 @@ cudaError_t launch_fused(DeviceInfo *d, int bit, const CUtensorMap &ta, const CU
         }
         if (CG == 2) max_groups = d->max_clusters[CG];
     }
+#ifdef TGEMM_TRACE
+    // Trace builds: run the persistent loop on fewer groups (timeline studies).
+    if (const char *g = std::getenv("TGEMM_TRACE_MAX_GROUPS")) max_groups = std::max(1, std::min(max_groups, std::atoi(g)));
+#endif
     const int groups = static_cast<int>(std::min<int64_t>(tiles, max_groups));
     if (CG == 1) {
         kernel<<<groups, kThreads, L::kDynamicBytes, s>>>(ta, tb, tc, p);
@@ -315,6 +343,12 @@ cudaError_t launch_fused(DeviceInfo *d, int bit, const CUtensorMap &ta, const CU
     return cudaLaunchKernelEx(&lc, kernel, ta, tb, tc, p);
 }
 
+// Work units of a plan: split-K pieces, whole tiles, narrow column parts.
+int64_t count_units(int64_t tiles, int split_k, int64_t split_first, int64_t narrow_first, int narrow_parts) {
+    const int64_t split_units = (split_k > 1) ? (tiles - split_first) * split_k : 0;
+    return split_units + narrow_first + (split_first - narrow_first) * narrow_parts;
+}
+
 // Fills the tile counts and instruction descriptor for `cfg` and launches.
 cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, const CUtensorMap &tb,
                           const CUtensorMap &tc, KParams p, cudaStream_t s, bool bf16) {
@@ -325,15 +359,31 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
     if (p.split_k < 1) p.split_k = 1;
     p.kb_per_split = static_cast<int>(cdiv(p.num_kb, p.split_k));
     p.split_k = static_cast<int>(cdiv(p.num_kb, p.kb_per_split));   // no empty k ranges
-    const int64_t units = tiles * p.split_k;
+    if (p.split_k == 1 || p.split_first < 0 || p.split_first > tiles) p.split_first = static_cast<int>(tiles);
+    if (p.narrow_parts < 1 || p.narrow_parts > max_narrow_parts(cfg) || p.narrow_first < 0 ||
+        p.narrow_first > p.split_first) {
+        p.narrow_parts = 1;
+        p.narrow_first = p.split_first;
+    }
+    if (p.narrow_parts == 1) p.narrow_first = p.split_first;
+    const int64_t split_units = (p.split_k > 1) ? (tiles - p.split_first) * p.split_k : 0;
+    const int64_t units = count_units(tiles, p.split_k, p.split_first, p.narrow_first, p.narrow_parts);
     if (units > INT32_MAX) return cudaErrorInvalidValue;
     p.num_tiles = static_cast<int>(tiles);
+    p.num_split_units = static_cast<int>(split_units);
     p.num_units = static_cast<int>(units);
     int group_m = 16;
     if (const char *g = std::getenv("TGEMM_GROUP_M")) group_m = std::max(1, std::atoi(g));
     p.group_m = std::min(p.num_m, group_m);
     p.idesc = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(cfg.bn),
                         p.a_mn != 0, p.b_kmajor == 0);
+    // Narrow units: MMA width bn / parts; with B stored [K, N] each CTA loads
+    // only its (bn / parts) / cg columns, with B stored [N, K] the whole box.
+    const int narrow_w = cfg.bn / p.narrow_parts;
+    p.idesc_narrow = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(narrow_w),
+                               p.a_mn != 0, p.b_kmajor == 0);
+    p.stage_tx_narrow = p.b_kmajor ? p.stage_tx
+                                   : static_cast<uint32_t>(kBM * kBK * 2 + (narrow_w / cfg.cg / 64) * 64 * kBK * 2);
     switch (cfg.bit) {
         case 1: return launch_fused<256, 4, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
         case 2: return launch_fused<128, 6, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
@@ -376,16 +426,35 @@ bool encode_maps(const Cfg &cfg, const void *a, int64_t lda, int ta, const void 
     return ok;
 }
 
-// Split-K for problems whose tiles cannot fill the GPU (small M, the decode
-// shapes): ranges of k per tile so that tiles x ranges about fills the SMs (or
-// SM pairs), each range at least 4 k-blocks, at most 16 ranges.
-int choose_split(const Cfg &cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
-    if (const char *f = std::getenv("TGEMM_SPLIT_K")) return std::max(1, std::atoi(f));
+// Work plan: which tiles are cut, and how.
+//  * Few tiles (under half the SMs / SM pairs; small M, the decode shapes):
+//    every tile's k loop is cut into ranges that about fill the GPU (split-K,
+//    reduced by the last range to finish; each range keeps at least 4
+//    k-blocks; at most 16 ranges).
+//  * Otherwise the tiles of the last, partial wave (the remainder after whole
+//    waves) are cut into column parts (narrow tail) so that the wave's work
+//    spreads over more SMs; they run last, which also shortens the last
+//    epilogue.
+struct Plan {
+    int split_k;
+    int64_t split_first;    // tiles from here on are split in k
+    int64_t narrow_first;   // tiles narrow_first .. split_first-1 are cut into columns
+    int narrow_parts;
+};
+
+Plan choose_plan(const Cfg &cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t groups = cfg.cg == 2 ? num_sms / 2 : num_sms;
     const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn);
     const int64_t kb = cdiv(K, kBK);
-    if (tiles * 2 > groups || kb < 8) return 1;
-    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({groups / tiles, kb / 4, 16})));
+    if (const char *f = std::getenv("TGEMM_SPLIT_K")) return {std::max(1, std::atoi(f)), 0, 0, 1};
+    if (kb >= 8 && tiles * 2 <= groups)
+        return {static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({groups / tiles, kb / 4, 16}))), 0, 0, 1};
+    const char *tail = std::getenv("TGEMM_TAIL_SPLIT");
+    const int64_t rem = tiles % groups;
+    if ((tail && std::atoi(tail) == 0) || rem == 0 || tiles < groups) return {1, tiles, tiles, 1};
+    const int s = narrow_parts_for(cfg, rem, groups);
+    if (s < 2) return {1, tiles, tiles, 1};
+    return {1, tiles, tiles - rem, s};
 }
 
 // fp32 partial floats per (tile, range): one region per epilogue warp of each CTA.
@@ -447,7 +516,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
         return st;
     }
 
-    const Cfg cfg = choose_config(M, N, d->num_sms);
+    const Cfg cfg = choose_config(M, N, K, d->num_sms);
     const bool tma_store = (ldc % 8) == 0;
     CUtensorMap tma, tmb, tmc;
     KParams p;
@@ -471,10 +540,15 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
 #ifdef TGEMM_TRACE
     p.trace = g_trace_buffer;
 #endif
-    // Split-K scratch: the fp32 partials and one zeroed counter per (tile, epilogue warp).
-    p.split_k = choose_split(cfg, M, N, K, d->num_sms);
+    // Split-K scratch: the fp32 partials and one zeroed counter per (split tile,
+    // CTA, epilogue warp).
+    const Plan plan = choose_plan(cfg, M, N, K, d->num_sms);
+    p.split_k = plan.split_k;
+    p.split_first = static_cast<int>(plan.split_first);
+    p.narrow_first = static_cast<int>(plan.narrow_first);
+    p.narrow_parts = plan.narrow_parts;
     if (p.split_k > 1) {
-        const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn);
+        const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn) - plan.split_first;
         const int64_t pbytes = tiles * p.split_k * partial_floats_per_unit(cfg) * 4;
         const int64_t cbytes = tiles * cfg.cg * kEpiWarps * 4;
         if (cudaMallocFromPoolAsync(&scratch_split, static_cast<size_t>(pbytes + cbytes), d->pool, stream) !=
@@ -595,7 +669,7 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
         b_use = scratch + b_off;
     }
 
-    const Cfg cfg = choose_config(M, N, d->num_sms);
+    const Cfg cfg = choose_config(M, N, K, d->num_sms);
     const bool tma_store = (ldc % 8) == 0;
     CUtensorMap tma, tmb, tmc;
     KParams p;
@@ -614,6 +688,12 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
+    // No split-K here (its partials would need scratch); the narrow tail needs none.
+    const Plan plan = choose_plan(cfg, M, N, K, d->num_sms);
+    if (plan.split_k == 1) {
+        p.narrow_first = static_cast<int>(plan.narrow_first);
+        p.narrow_parts = plan.narrow_parts;
+    }
     const cudaError_t e = launch_config(d, cfg, tma, tmb, tmc, p, stream, bf16);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -851,7 +931,32 @@ extern "C" tgemm_status tgemm_last_device_status(void) {
 
 extern "C" int tgemm_version(void) { return kVersion; }
 
+extern "C" tgemm_status tgemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int32_t *out) {
+    if (out == nullptr || M < 1 || N < 1 || K < 1 || num_sms < 2 || M > INT32_MAX || N > INT32_MAX ||
+        K > INT32_MAX)
+        return TGEMM_ERR_INVALID_ARG;
+    const Cfg cfg = choose_config(M, N, K, num_sms);
+    Plan plan = choose_plan(cfg, M, N, K, num_sms);
+    const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn);
+    // The same normalisation as the launch.
+    int split_k = std::max(1, plan.split_k);
+    const int64_t kb = cdiv(K, kBK);
+    split_k = static_cast<int>(cdiv(kb, cdiv(kb, split_k)));
+    int64_t split_first = plan.split_first;
+    if (split_k == 1 || split_first < 0 || split_first > tiles) split_first = tiles;
+    int64_t narrow_first = plan.narrow_first;
+    int parts = plan.narrow_parts;
+    if (parts < 1 || parts > max_narrow_parts(cfg) || narrow_first < 0 || narrow_first > split_first) parts = 1;
+    if (parts == 1) narrow_first = split_first;
+    const int64_t units = count_units(tiles, split_k, split_first, narrow_first, parts);
+    if (tiles > INT32_MAX || units > INT32_MAX) return TGEMM_ERR_INVALID_ARG;
+    const int64_t groups = std::min<int64_t>(units, num_sms / cfg.cg);
+    const int64_t v[10] = {cfg.bn, cfg.cg, cfg.stages, tiles, groups, split_k, split_first, narrow_first, parts, units};
+    for (int i = 0; i < 10; ++i) out[i] = static_cast<int32_t>(v[i]);
+    return TGEMM_OK;
+}
+
 #ifdef TGEMM_TRACE
-// Trace builds only: the device buffer the kernels stamp into (8 CTAs x 64).
+// Trace builds only: the device buffer the kernels stamp into (10240 + 384 words).
 extern "C" void tgemm_trace_set_buffer(unsigned long long *dev_ptr) { g_trace_buffer = dev_ptr; }
 #endif

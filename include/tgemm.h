@@ -95,7 +95,9 @@ typedef enum {
  * shapes) split the k loop of each tile across CTAs: fp32 partial sums go to
  * pool scratch and the last CTA to finish a tile region adds them in a fixed
  * order before the epilogue, so results are deterministic; they may differ
- * in the last bits from an unsplit run (different summation order).
+ * in the last bits from an unsplit run (different summation order).  Larger
+ * problems whose tiles leave a last, partial wave cut those tiles into
+ * narrower column parts instead; that changes no result bit.
  *
  * Asynchrony: returns once the work is enqueued; the caller synchronises.
  * Thread safety: safe to call from several host threads.
@@ -194,6 +196,29 @@ tgemm_status tgemm_last_device_status(void);
 
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int tgemm_version(void);
+
+/*
+ * tgemm_plan — the work plan tgemm_run (and tgemm_run_ex / tgemm_run_host per
+ * chunk) uses for an M x N x K problem on a GPU with num_sms SMs.  Host logic
+ * only: no device is touched, so it also answers on a machine without a GPU.
+ * The transposed layouts do not change the plan; tgemm_run_noalloc uses it
+ * with split_k forced to 1.
+ *
+ * out (caller-owned, 10 int32 entries):
+ *   [0] tile width BN (columns)      [1] CTAs per tile (1, or 2 for a pair: 256 rows)
+ *   [2] shared-memory ring stages    [3] tiles = ceil(M / (128 * [1])) * ceil(N / BN)
+ *   [4] persistent CTA groups launched (CTAs = [4] * [1])
+ *   [5] split_k (1: no k split)      [6] first tile split in k (tiles from here on)
+ *   [7] first narrow tile            [8] column parts of each narrow tile (1: none);
+ *                                        tiles [7] .. [6]-1 are cut into [8] parts
+ *   [9] work units of the persistent loop
+ *
+ * The tile-shape rule and the plan are heuristics: they may change between
+ * versions without changing any result beyond the split-K note of tgemm_run.
+ * Returns TGEMM_ERR_INVALID_ARG if out is NULL, num_sms < 2, or a size is
+ * below 1 or above INT32_MAX; TGEMM_OK otherwise.
+ */
+tgemm_status tgemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int32_t *out);
 
 #ifdef __cplusplus
 }
