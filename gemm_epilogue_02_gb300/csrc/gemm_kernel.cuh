@@ -95,6 +95,7 @@ struct KParams {
     unsigned int *counters;
     int a_mn;                  // A stored transposed ([K, M], M contiguous): MN-major operand
     int b_kmajor;              // B stored transposed ([N, K], K contiguous): K-major operand
+    int b_3d;                  // B [K, N] through a 3-D map: all BN/CG columns of a k-block in one box
     uint32_t stage_tx;         // bytes one CTA loads per ring stage (depends on the layouts)
     uint32_t idesc;
     unsigned int *status;      // device status word
@@ -109,7 +110,7 @@ struct KParams {
 // i < 8: 8+4i first MMA issued, 9+4i last MMA committed, 10+4i epilogue start
 // (warp 2), 11+4i epilogue stores issued (warp 2); first unit split in k:
 // 40 partials written, 41 fence done, 42 counter taken, 43 arrival index + 1,
-// 44 reduction done (last arriver only).  The buffer holds 10240 + 384 words.
+// 44 reduction done (last arriver only).  The buffer holds 10240 + 448 words.
 #ifdef TGEMM_TRACE
 #define TGEMM_STAMP(slot)                                                                         \
     do {                                                                                          \
@@ -118,7 +119,7 @@ struct KParams {
 // Stage timeline (SM clock cycles) of CTA 0 for the second unit's first 64
 // k-blocks: p.trace[10240 + kind * 64 + i], kind 0 producer before the empty
 // wait, 1 producer past it, 2 producer loads issued, 3 MMA before the full
-// wait, 4 MMA past it, 5 MMA commit issued.
+// wait, 4 MMA past it, 5 MMA commit issued, 6 producer past its expect-tx.
 #define TGEMM_STAGE_STAMP(kind, i)                                                           \
     do {                                                                                     \
         if (blockIdx.x == 0 && (i) >= 0 && (i) < 64)                                         \
@@ -282,11 +283,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int BN, int STAGES, int CG>
+// KSUB: k-blocks per ring slot.  A slot has one full and one empty barrier and
+// KSUB stage buffers; the MMA lane waits once per slot (each wait costs the
+// lane a shared-memory round trip during which it issues nothing).
+template <int BN, int STAGES, int CG, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     tgemm_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC, const KParams p) {
     using L = Smem<BN, STAGES, CG>;
+    static_assert(KSUB >= 1 && STAGES % KSUB == 0, "whole slots");
+    constexpr int NSLOT = STAGES / KSUB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
@@ -322,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto leader_tempty = [&](int a) { return (CG == 2) ? mapa_shared(tempty_bar(a), 0) : tempty_bar(a); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NSLOT; ++s) {
             mbar_init(full_bar(s), 1);             // rank 0's expect-tx arrival (bytes of the whole group)
             mbar_init(empty_bar(s), 1);
         }
@@ -354,10 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int stage = 0;
+            int slot = 0;
             uint32_t phase = 0;
-            uint32_t uses[STAGES];
-            for (int s = 0; s < STAGES; ++s) uses[s] = 0;
+            uint32_t uses[NSLOT];
+            for (int s = 0; s < NSLOT; ++s) uses[s] = 0;
             bool ok = true;
             for (int u = group_id; u < p.num_units && ok; u += num_groups) {
                 const Unit w = unit_info(u, p, BN);
@@ -370,49 +376,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b_sub = narrow ? (w.width / CG) / 64 : L::kBSub;
                 const uint32_t tx = narrow ? p.stage_tx_narrow : p.stage_tx;
                 const bool st_trace = (u == group_id + num_groups);
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                // A unit starts on a slot boundary; its last slot may hold fewer k-blocks.
+                for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
+                    const int nkb = min(KSUB, w.kb1 - kb);
                     if (st_trace) TGEMM_STAGE_STAMP(0, kb - w.kb0);
-                    if (!wait_bar<true>(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                    if (!wait_bar<true>(empty_bar(slot), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                     if (st_trace) TGEMM_STAGE_STAMP(1, kb - w.kb0);
-                    const uint32_t a_dst = sbase + L::kOffA + stage * L::kABytes;
-                    const uint32_t b_dst = sbase + L::kOffB + stage * L::kBBytes;
                     // Rank 0 announces the bytes of the whole group; with a CTA pair the
                     // peer's copies report to rank 0's barrier (its transaction count may
                     // dip below zero until the announcement lands, which is allowed).
-                    const uint32_t fb = (CG == 1) ? full_bar(stage) : leader_full(stage);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), CG * tx);
+                    const uint32_t fb = (CG == 1) ? full_bar(slot) : leader_full(slot);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), CG * tx * static_cast<uint32_t>(nkb));
+                    if (st_trace) TGEMM_STAGE_STAMP(6, kb - w.kb0);
                     auto load = [&](uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y) {
                         if constexpr (CG == 1) tma_load_2d(dst, m, fb, x, y);
                         else tma_load_2d_pair(dst, m, fb, x, y);
                     };
-                    if (!p.a_mn) {
-                        // A [M, K]: one box of 128 rows x 64 k (K-major, 128-byte rows).
-                        load(a_dst, &tmA, kb * kBK, a_row);
-                    } else {
-                        // A stored [K, M]: two boxes of 64 k-rows x 64 m (MN-major).
 #pragma unroll
-                        for (int j = 0; j < kBM / 64; ++j)
-                            load(a_dst + j * (kBK * 128), &tmA, a_row + j * 64, kb * kBK);
-                    }
-                    if (!p.b_kmajor) {
-                        // B [K, N]: 64-column sub-tiles of 64 k-rows (MN-major).
+                    for (int i = 0; i < KSUB; ++i) {
+                        if (i >= nkb) break;
+                        const int stage = slot * KSUB + i;
+                        const int k0 = (kb + i) * kBK;
+                        const uint32_t a_dst = sbase + L::kOffA + stage * L::kABytes;
+                        const uint32_t b_dst = sbase + L::kOffB + stage * L::kBBytes;
+                        if (!p.a_mn) {
+                            // A [M, K]: one box of 128 rows x 64 k (K-major, 128-byte rows).
+                            load(a_dst, &tmA, k0, a_row);
+                        } else {
+                            // A stored [K, M]: two boxes of 64 k-rows x 64 m (MN-major).
 #pragma unroll
-                        for (int j = 0; j < L::kBSub; ++j)
-                            if (j < b_sub) load(b_dst + j * (kBK * 128), &tmB, b_col + j * 64, kb * kBK);
-                    } else {
-                        // B stored [N, K]: one box of BN/CG n-rows x 64 k (K-major); a
-                        // narrow unit's MMA reads only the first width / CG of them.
-                        load(b_dst, &tmB, kb * kBK, b_col);
+                            for (int j = 0; j < kBM / 64; ++j)
+                                load(a_dst + j * (kBK * 128), &tmA, a_row + j * 64, k0);
+                        }
+                        if (p.b_3d) {
+                            // B [K, N] viewed as (64 columns, K rows, column chunks): one box
+                            // holds the kBSub 64-column sub-tiles of 64 k-rows (MN-major),
+                            // laid out as the 2-D copies would place them.
+                            if constexpr (CG == 1) tma_load_3d(b_dst, &tmB, fb, 0, k0, b_col >> 6);
+                            else tma_load_3d_pair(b_dst, &tmB, fb, 0, k0, b_col >> 6);
+                        } else if (!p.b_kmajor) {
+                            // B [K, N]: 64-column sub-tiles of 64 k-rows (MN-major).
+#pragma unroll
+                            for (int j = 0; j < L::kBSub; ++j)
+                                if (j < b_sub) load(b_dst + j * (kBK * 128), &tmB, b_col + j * 64, k0);
+                        } else {
+                            // B stored [N, K]: one box of BN/CG n-rows x 64 k (K-major); a
+                            // narrow unit's MMA reads only the first width / CG of them.
+                            load(b_dst, &tmB, k0, b_col);
+                        }
                     }
                     if (st_trace) TGEMM_STAGE_STAMP(2, kb - w.kb0);
-                    ++uses[stage];
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    ++uses[slot];
+                    if (++slot == NSLOT) { slot = 0; phase ^= 1u; }
                 }
             }
             if (!ok) {
                 // Let every copy this thread started land before the CTA exits.
                 if (CG == 1 || rank == 0) {
-                    for (int s = 0; s < STAGES; ++s)
+                    for (int s = 0; s < NSLOT; ++s)
                         if (uses[s]) drain_wait(full_bar(s), (uses[s] - 1u) & 1u);
                 } else {
                     // The peer's copies report to rank 0's barriers: give them time to land.
@@ -425,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
-            int stage = 0;
+            int slot = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
@@ -451,22 +472,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * L::kAccStride;
                 uint32_t accumulate = 0u;   // the unit's first MMA overwrites the accumulator
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = kb0; kb < kb1; kb += KSUB) {
+                    const int nkb = min(KSUB, kb1 - kb);
                     if (tile_i == 1) TGEMM_STAGE_STAMP(3, kb - kb0);
-                    if (!wait_bar<false>(full_bar(stage), phase, abort_flag, p.status)) { ok = false; break; }
+                    if (!wait_bar<false>(full_bar(slot), phase, abort_flag, p.status)) { ok = false; break; }
                     if (tile_i == 1) TGEMM_STAGE_STAMP(4, kb - kb0);
                     tc_fence_after();
                     if (kb == kb0 && tile_i < 8) TGEMM_STAMP(8 + 4 * tile_i);
-                    const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (L::kABytes >> 4);
-                    const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (L::kBBytes >> 4);
+                    const uint32_t first = static_cast<uint32_t>(slot * KSUB);
+                    const uint64_t ad = a_desc0 + first * (L::kABytes >> 4);
+                    const uint64_t bd = b_desc0 + first * (L::kBBytes >> 4);
                     mma_f16_ss<CG>(d_tmem, ad, bd, idesc, accumulate);
 #pragma unroll
                     for (int k = 1; k < kBK / kUmmaK; ++k)
                         mma_f16_ss<CG>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
+#pragma unroll
+                    for (int i = 1; i < KSUB; ++i) {
+                        if (i >= nkb) break;
+                        const uint64_t adi = ad + static_cast<uint32_t>(i) * (L::kABytes >> 4);
+                        const uint64_t bdi = bd + static_cast<uint32_t>(i) * (L::kBBytes >> 4);
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k)
+                            mma_f16_ss<CG>(d_tmem, adi + k * a_kstep, bdi + k * b_kstep, idesc, 1u);
+                    }
                     accumulate = 1u;
-                    mma_commit<CG>(empty_bar(stage));      // frees the ring stage once read
+                    mma_commit<CG>(empty_bar(slot));       // frees the ring slot once read
                     if (tile_i == 1) TGEMM_STAGE_STAMP(5, kb - kb0);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (++slot == NSLOT) { slot = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 mma_commit<CG>(tfull_bar(acc));            // accumulator ready for the epilogue

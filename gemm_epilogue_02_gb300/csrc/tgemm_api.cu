@@ -198,6 +198,26 @@ bool make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int6
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// B [K, N] (pitch ld) as a 3-D tensor (64 columns, K rows, ceil(N / 64) column
+// chunks; strides ld * 2 and 128 bytes) with a box of 64 x 64 x `chunks`: one
+// copy lands `chunks` 64-column sub-tiles of 64 k-rows, 8 KiB apart, exactly as
+// that many 2-D copies would.  The last chunk may run past column N up to
+// round_up(N, 64): the caller uses it only when those columns lie inside each
+// row's pitch (they then only feed output columns that are never stored).
+bool make_map_b3d(CUtensorMap *m, const void *base, int64_t K, int64_t N, int64_t ld, uint32_t chunks,
+                  bool bf16) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(K), static_cast<cuuint64_t>((N + 63) / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBK), chunks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- configs
 // A configuration: C tile = (128 * cg) x bn, `stages` ring stages, cg CTAs per tile.
 struct Cfg {
@@ -282,11 +302,11 @@ Cfg choose_config(int64_t M, int64_t N, int64_t K, int num_sms) {
     return best;
 }
 
-template <int BN, int ST, int CG>
+template <int BN, int ST, int CG, int KSUB>
 cudaError_t launch_fused(DeviceInfo *d, int bit, const CUtensorMap &ta, const CUtensorMap &tb,
                          const CUtensorMap &tc, const KParams &p, int64_t tiles, cudaStream_t s) {
     using L = Smem<BN, ST, CG>;
-    auto kernel = tgemm_fused_kernel<BN, ST, CG>;
+    auto kernel = tgemm_fused_kernel<BN, ST, CG, KSUB>;
     int max_groups = d->num_sms;
     {
         std::lock_guard<std::mutex> g(d->mu);
@@ -382,16 +402,18 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
     const int narrow_w = cfg.bn / p.narrow_parts;
     p.idesc_narrow = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(narrow_w),
                                p.a_mn != 0, p.b_kmajor == 0);
-    p.stage_tx_narrow = p.b_kmajor ? p.stage_tx
-                                   : static_cast<uint32_t>(kBM * kBK * 2 + (narrow_w / cfg.cg / 64) * 64 * kBK * 2);
+    // (A 3-D B box always carries all bn / cg columns.)
+    p.stage_tx_narrow = (p.b_kmajor || p.b_3d)
+                            ? p.stage_tx
+                            : static_cast<uint32_t>(kBM * kBK * 2 + (narrow_w / cfg.cg / 64) * 64 * kBK * 2);
     switch (cfg.bit) {
-        case 1: return launch_fused<256, 4, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 2: return launch_fused<128, 6, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 4: return launch_fused<64, 8, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 8: return launch_fused<256, 6, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 16: return launch_fused<128, 8, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 32: return launch_fused<192, 4, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
-        default: return launch_fused<224, 6, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 1: return launch_fused<256, 4, 1, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 2: return launch_fused<128, 6, 1, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 4: return launch_fused<64, 8, 1, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 8: return launch_fused<256, 6, 2, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 16: return launch_fused<128, 8, 2, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 32: return launch_fused<192, 4, 1, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
+        default: return launch_fused<224, 6, 2, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
     }
 }
 
@@ -414,13 +436,21 @@ bool encode_maps(const Cfg &cfg, const void *a, int64_t lda, int ta, const void 
                  CUtensorMap *tma, CUtensorMap *tmb, CUtensorMap *tmc, KParams *p) {
     const int bcols = cfg.bn / cfg.cg;
     std::memset(tmc, 0, sizeof(*tmc));
+    // One 3-D copy per k-block for B [K, N] when every CTA's columns start on a
+    // 64-column boundary and the last chunk's columns past N stay inside B's
+    // rows (B is a K x ldb array; see the header).
+    const bool b3d_ok = !tb && cfg.bn % 64 == 0 && bcols % 64 == 0 &&
+                        (N % 64 == 0 || ldb >= cdiv(N, 64) * 64) && std::getenv("TGEMM_NO_B3D") == nullptr;
+    bool b3d = b3d_ok && make_map_b3d(tmb, b, K, N, ldb, static_cast<uint32_t>(bcols / 64), bf16);
+    if (!b3d) std::memset(tmb, 0, sizeof(*tmb));
     const bool ok =
         (ta ? make_map(tma, a, K, M, lda, 64, kBK, bf16) : make_map(tma, a, M, K, lda, kBK, kBM, bf16)) &&
-        (tb ? make_map(tmb, b, N, K, ldb, kBK, static_cast<uint32_t>(bcols), bf16)
-            : make_map(tmb, b, K, N, ldb, 64, kBK, bf16)) &&
+        (b3d || (tb ? make_map(tmb, b, N, K, ldb, kBK, static_cast<uint32_t>(bcols), bf16)
+                    : make_map(tmb, b, K, N, ldb, 64, kBK, bf16))) &&
         (!tma_store || make_map(tmc, C, M, N, ldc, static_cast<uint32_t>(cfg.cw()), 32, bf16));
     p->a_mn = ta;
     p->b_kmajor = tb;
+    p->b_3d = b3d ? 1 : 0;
     p->stage_tx = static_cast<uint32_t>(kBM * kBK * 2 +
                                         (tb ? bcols * kBK * 2 : cdiv(bcols, 64) * 64 * kBK * 2));
     return ok;
@@ -957,6 +987,6 @@ extern "C" tgemm_status tgemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
 }
 
 #ifdef TGEMM_TRACE
-// Trace builds only: the device buffer the kernels stamp into (10240 + 384 words).
+// Trace builds only: the device buffer the kernels stamp into (10240 + 448 words).
 extern "C" void tgemm_trace_set_buffer(unsigned long long *dev_ptr) { g_trace_buffer = dev_ptr; }
 #endif

@@ -90,6 +90,15 @@ typedef enum {
  * scratch buffer drawn stream-ordered from a library-owned memory pool and
  * returned to it on `stream`; when ldc is not a multiple of 8 the epilogue
  * stores C with plain masked stores instead of tensor-memory-access stores.
+ * The library may read (never write) any element of the declared input
+ * arrays, pitch padding included: a padded element only ever feeds outputs
+ * outside C's M x N, which are not stored.
+ *
+ * Environment overrides of the work plan, for testing and tuning only (results
+ * change at most by the split-K note below): TGEMM_FORCE_CFG (tile shape:
+ * 256, 192, 128, 64, 256x2, 224x2, 128x2), TGEMM_SPLIT_K (k ranges for every
+ * tile), TGEMM_TAIL_SPLIT=0 (no narrow tail), TGEMM_GROUP_M (row-blocks per
+ * column sweep), TGEMM_NO_B3D (one copy per 64-column sub-tile of B).
  *
  * Problems with too few output tiles to fill the GPU (few rows, e.g. decode
  * shapes) split the k loop of each tile across CTAs: fp32 partial sums go to

@@ -202,6 +202,26 @@ def test_narrow_tail(cuda_lib, monkeypatch, cfg, M, N, K, parts):
     assert np.array_equal(got, whole), "narrow parts changed the result bits"
 
 
+@pytest.mark.parametrize("cfg", ["256x2", "128x2", "256", "192", "128", "64"])
+@pytest.mark.parametrize("M,N,K,ldb", [(700, 1024, 300, None),     # N a multiple of 64: one 3-D box per k-block
+                                       (700, 1000, 300, 1024),     # last chunk past N inside the pitch
+                                       (700, 1000, 300, None)])    # ... outside it: 2-D copies
+def test_b_sub_tiles_in_one_copy(cuda_lib, monkeypatch, cfg, M, N, K, ldb):
+    """B [K, N] loaded as one 3-D box per k-block (all 64-column sub-tiles of a
+    CTA) gives the same bits as one 2-D copy per sub-tile, and exact integers."""
+    monkeypatch.setenv("TGEMM_FORCE_CFG", cfg)
+    inputs, got = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=61, kind="int", ldb=ldb)
+    assert_bit_exact(got[:, :N], oracle_ref(inputs, M, N, K, "fp16", "bias_relu"), "fp16", f"{cfg} b3d")
+    monkeypatch.setenv("TGEMM_NO_B3D", "1")
+    _, two_d = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=61, kind="int", ldb=ldb)
+    assert np.array_equal(got, two_d)
+    inputs, got = run_tgemm(cuda_lib, M, N, K, "bf16", "bias_gelu", seed=62, kind="gelu", ldb=ldb)
+    monkeypatch.delenv("TGEMM_NO_B3D")
+    _, three_d = run_tgemm(cuda_lib, M, N, K, "bf16", "bias_gelu", seed=62, kind="gelu", ldb=ldb)
+    assert np.array_equal(got, three_d)
+    check_epilogue(three_d[:, :N], inputs, M, N, K, "bf16", "bias_gelu", f"{cfg} b3d gelu")
+
+
 @pytest.mark.parametrize("ta,tb", [(0, 1), (1, 0)])
 def test_narrow_tail_transposed(cuda_lib, monkeypatch, ta, tb):
     """Narrow parts with B stored [N, K] (the whole n box is loaded, the MMA
