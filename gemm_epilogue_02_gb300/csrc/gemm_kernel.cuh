@@ -110,7 +110,7 @@ struct KParams {
 // i < 8: 8+4i first MMA issued, 9+4i last MMA committed, 10+4i epilogue start
 // (warp 2), 11+4i epilogue stores issued (warp 2); first unit split in k:
 // 40 partials written, 41 fence done, 42 counter taken, 43 arrival index + 1,
-// 44 reduction done (last arriver only).  The buffer holds 10240 + 448 words.
+// 44 reduction done (last arriver only).  The buffer holds 10240 + 480 words.
 #ifdef TGEMM_TRACE
 #define TGEMM_STAMP(slot)                                                                         \
     do {                                                                                          \
@@ -125,7 +125,19 @@ struct KParams {
         if (blockIdx.x == 0 && (i) >= 0 && (i) < 64)                                         \
             p.trace[10240 + (kind) * 64 + (i)] = clock64();                                  \
     } while (0)
+// Epilogue timeline (SM clock cycles) of warp 2 of CTA 0 for its second unit:
+// p.trace[10688 + i], i = 0 accumulator ready, 1 bias handed over, 2 first
+// TMEM load landed, 3 + 2s sub-chunk s processed, 4 + 2s next load landed,
+// 20 done, 24 + s sub-chunk s's values packed, 28 + s its staging written.
+#define TGEMM_EPI_STAMP(i)                                                                   \
+    do {                                                                                     \
+        if (blockIdx.x == 0 && warp == 2 && lane == 0 && tile_i == 1 && (i) < 32)            \
+            p.trace[10688 + (i)] = clock64();                                                \
+    } while (0)
 #else
+#define TGEMM_EPI_STAMP(i) \
+    do {                   \
+    } while (0)
 #define TGEMM_STAMP(slot) \
     do {                  \
     } while (0)
@@ -250,11 +262,6 @@ __device__ __forceinline__ Unit unit_info(int u, const KParams &p, int bn) {
     return w;
 }
 
-__device__ __forceinline__ float bias_val(const void *bias, int idx, int is_bf16) {
-    const unsigned short raw = __ldg(reinterpret_cast<const unsigned short *>(bias) + idx);
-    return is_bf16 ? __bfloat162float(__ushort_as_bfloat16(raw)) : __half2float(__ushort_as_half(raw));
-}
-
 __device__ __forceinline__ float epi_relu(float v) {
     // x <= 0 (incl. -0.0) -> +0.0; NaN compares false and is kept.
     return (v <= 0.0f) ? 0.0f : v;
@@ -268,19 +275,49 @@ __device__ __forceinline__ float epi_gelu(float x) {
     return __fdividef(x, 1.0f + __expf(-u));
 }
 
-__device__ __forceinline__ float epi_act(float v, int act) {
-    if (act == 1) return epi_relu(v);
-    if (act == 2) return epi_gelu(v);
-    return v;
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi, int is_bf16) {
-    if (is_bf16) {
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (kBf16) {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
         return *reinterpret_cast<uint32_t *>(&h);
+    } else {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
     }
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// The epilogue arithmetic of 32 consecutive columns of one row: fp32 sum +
+// bias (16-bit values, four uint4 of the warp's strip), activation, one
+// rounding to the output format, packed in pairs into out[0..15].  Specialised
+// on the format and the activation so that the unrolled body has no branches.
+template <bool kBf16, int kAct>
+__device__ __forceinline__ void epi_math32(const uint32_t (&r)[32], const uint4 *bsrc, uint32_t *out) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const uint4 raw = bsrc[g];
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float b0, b1;
+            if constexpr (kBf16) {
+                b0 = __uint_as_float(w[h] << 16);            // bf16 -> fp32 is exact
+                b1 = __uint_as_float(w[h] & 0xFFFF0000u);
+            } else {
+                b0 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[h] & 0xFFFFu)));
+                b1 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[h] >> 16)));
+            }
+            float v0 = __uint_as_float(r[g * 8 + 2 * h]) + b0;
+            float v1 = __uint_as_float(r[g * 8 + 2 * h + 1]) + b1;
+            if constexpr (kAct == 1) {
+                v0 = epi_relu(v0);
+                v1 = epi_relu(v1);
+            } else if constexpr (kAct == 2) {
+                v0 = epi_gelu(v0);
+                v1 = epi_gelu(v1);
+            }
+            out[g * 4 + h] = pack2<kBf16>(v0, v1);
+        }
+    }
 }
 
 // KSUB: k-blocks per ring slot.  A slot has one full and one empty barrier and
@@ -512,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         constexpr int CW = L::kCW;               // columns per chunk: 64 (128-byte rows) or 32 (64-byte rows)
+        const int math_mode = (p.is_bf16 ? 3 : 0) + p.act;   // epi_math32 specialisation
         constexpr int kRowBytes = CW * 2;
         const int ew = warp - 2;                 // epilogue warp index 0..kEpiWarps-1
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
@@ -565,13 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             if (warp == 2 && lane == 0 && tile_i < 8) TGEMM_STAMP(10 + 4 * tile_i);
-            // Publish this tile's bias strip, then start fetching the next tile's.
-            __syncwarp();
-#pragma unroll
-            for (int k = 0; k < kBiasPerLane; ++k)
-                if (lane + 32 * k < static_cast<int>(L::kBiasCols)) bias_s[lane + 32 * k] = bias_next[k];
-            __syncwarp();
-            if (u + num_groups < p.num_units) fetch_bias(u + num_groups);
+            TGEMM_EPI_STAMP(0);
             const int m0 = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM + q * 32;
             const int n_tile = n_blk * BN + w.col0;     // accumulator column 0 is C column n_tile
             // Only chunks / rows that intersect C are read out and stored (no
@@ -587,6 +619,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto tload = [&](int sub, uint32_t (&r)[32]) {
                 tmem_ld_32x32b_x32(tbase + static_cast<uint32_t>(chunk_of(sub) * CW + 32 * (sub % SUBS)), r);
             };
+            uint32_t ra[32], rb[32];
+            // The unit's first TMEM load goes out before the bias hand-over,
+            // which then hides its latency.
+            if (split < 0 && n_sub > 0) tload(0, ra);
+            // Publish this unit's bias strip, then start fetching the next unit's.
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < kBiasPerLane; ++k)
+                if (lane + 32 * k < static_cast<int>(L::kBiasCols)) bias_s[lane + 32 * k] = bias_next[k];
+            __syncwarp();
+            if (u + num_groups < p.num_units) fetch_bias(u + num_groups);
+            TGEMM_EPI_STAMP(1);
             uint32_t packed[CW / 2];
             // + bias and activation for sub-chunk H of a chunk, one rounding into
             // `packed`; after the last sub-chunk, swizzled staging and the store.
@@ -596,32 +640,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n0 = n_tile + c * CW;
                 // Bias of these 32 columns from the warp's strip (broadcast reads).
                 const uint4 *bsrc = reinterpret_cast<const uint4 *>(bias_s + ((sub / SUBS) * CW + 32 * H));
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const uint4 raw = bsrc[g];
-                    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                    float bv[8];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const unsigned short lo = static_cast<unsigned short>(w[h] & 0xFFFFu);
-                        const unsigned short hi = static_cast<unsigned short>(w[h] >> 16);
-                        if (p.is_bf16) {
-                            bv[2 * h] = __bfloat162float(__ushort_as_bfloat16(lo));
-                            bv[2 * h + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
-                        } else {
-                            bv[2 * h] = __half2float(__ushort_as_half(lo));
-                            bv[2 * h + 1] = __half2float(__ushort_as_half(hi));
-                        }
-                    }
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        float v0 = __uint_as_float(r[g * 8 + 2 * h]) + bv[2 * h];
-                        float v1 = __uint_as_float(r[g * 8 + 2 * h + 1]) + bv[2 * h + 1];
-                        v0 = epi_act(v0, p.act);
-                        v1 = epi_act(v1, p.act);
-                        packed[16 * H + g * 4 + h] = pack2(v0, v1, p.is_bf16);
-                    }
+                uint32_t *out = packed + 16 * H;
+                switch (math_mode) {
+                    case 0: epi_math32<false, 0>(r, bsrc, out); break;
+                    case 1: epi_math32<false, 1>(r, bsrc, out); break;
+                    case 2: epi_math32<false, 2>(r, bsrc, out); break;
+                    case 3: epi_math32<true, 0>(r, bsrc, out); break;
+                    case 4: epi_math32<true, 1>(r, bsrc, out); break;
+                    default: epi_math32<true, 2>(r, bsrc, out); break;
                 }
+                TGEMM_EPI_STAMP(24 + (sub & 3));
                 if constexpr (H != SUBS - 1) return;
                 // Stage the 32 x CW block: row `lane`, swizzled 16-byte chunks.
                 const uint32_t sb = cstage0 + buf * L::kCStageBytes;
@@ -642,6 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  "r"(packed[4 * j + 3])
                                  : "memory");
                 }
+                TGEMM_EPI_STAMP(28 + (sub & 3));
                 if (use_tma) {
                     fence_proxy_async_shared();
                     __syncwarp();
@@ -690,11 +719,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     release_acc(acc);
                 } else {
                     float *mine = region(split);
-                    uint32_t ra[32];
 #pragma unroll 1
                     for (int sub = 0; sub < n_sub; ++sub) {
                         tload(sub, ra);
-                        tmem_wait_ld();
+                        tmem_wait_ld(ra);
                         if (sub == n_sub - 1) release_acc(acc);
 #pragma unroll
                         for (int g = 0; g < 8; ++g)
@@ -753,27 +781,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the accumulator goes back to the MMA lane as soon as its last load
                 // lands.  Sub-chunks alternate between ra (even: first half of a chunk)
                 // and rb (odd: second half when a chunk has two).
-                uint32_t ra[32], rb[32];
                 int sub = 0;
-                tload(sub, ra);
-                tmem_wait_ld();
+                tmem_wait_ld(ra);                        // the load issued at the unit's start
+                TGEMM_EPI_STAMP(2);
 #pragma unroll 1
                 for (;;) {
                     bool more = sub + 1 < n_sub;
                     if (more) tload(sub + 1, rb);
                     else release_acc(acc);
                     process(std::integral_constant<int, 0>{}, sub, ra);
+                    TGEMM_EPI_STAMP(3 + 2 * sub);
                     if (!more) break;
-                    tmem_wait_ld();
+                    tmem_wait_ld(rb);
+                    TGEMM_EPI_STAMP(4 + 2 * sub);
                     ++sub;
                     more = sub + 1 < n_sub;
                     if (more) tload(sub + 1, ra);
                     else release_acc(acc);
                     process(std::integral_constant<int, SUBS - 1>{}, sub, rb);
+                    TGEMM_EPI_STAMP(3 + 2 * sub);
                     if (!more) break;
-                    tmem_wait_ld();
+                    tmem_wait_ld(ra);
+                    TGEMM_EPI_STAMP(4 + 2 * sub);
                     ++sub;
                 }
+                TGEMM_EPI_STAMP(20);
             }
             if (warp == 2 && lane == 0 && tile_i < 8) TGEMM_STAMP(11 + 4 * tile_i);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }

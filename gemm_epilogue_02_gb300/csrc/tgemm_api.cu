@@ -987,6 +987,6 @@ extern "C" tgemm_status tgemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
 }
 
 #ifdef TGEMM_TRACE
-// Trace builds only: the device buffer the kernels stamp into (10240 + 448 words).
+// Trace builds only: the device buffer the kernels stamp into (10240 + 480 words).
 extern "C" void tgemm_trace_set_buffer(unsigned long long *dev_ptr) { g_trace_buffer = dev_ptr; }
 #endif
