@@ -95,7 +95,8 @@ struct KParams {
     unsigned int *counters;
     int a_mn;                  // A stored transposed ([K, M], M contiguous): MN-major operand
     int b_kmajor;              // B stored transposed ([N, K], K contiguous): K-major operand
-    int b_3d;                  // B [K, N] through a 3-D map: all BN/CG columns of a k-block in one box
+    int b_3d;                  // B [K, N] through a 3-D map (tmB): all BN/CG columns of a k-block in
+                               // one box; narrow units then use the 2-D map tmB2
     uint32_t stage_tx;         // bytes one CTA loads per ring stage (depends on the layouts)
     uint32_t idesc;
     unsigned int *status;      // device status word
@@ -326,6 +327,7 @@ __device__ __forceinline__ void epi_math32(const uint32_t (&r)[32], const uint4 
 template <int BN, int STAGES, int CG, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     tgemm_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmB2,
                        const __grid_constant__ CUtensorMap tmC, const KParams p) {
     using L = Smem<BN, STAGES, CG>;
     static_assert(KSUB >= 1 && STAGES % KSUB == 0, "whole slots");
@@ -381,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if (p.b_3d) prefetch_tmap(&tmB2);
         if (p.tma_store) prefetch_tmap(&tmC);
     }
     if constexpr (CG == 2) cluster_sync();       // the peer is running and its barriers exist
@@ -445,17 +448,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int j = 0; j < kBM / 64; ++j)
                                 load(a_dst + j * (kBK * 128), &tmA, a_row + j * 64, k0);
                         }
-                        if (p.b_3d) {
+                        if (p.b_3d && !narrow) {
                             // B [K, N] viewed as (64 columns, K rows, column chunks): one box
                             // holds the kBSub 64-column sub-tiles of 64 k-rows (MN-major),
                             // laid out as the 2-D copies would place them.
                             if constexpr (CG == 1) tma_load_3d(b_dst, &tmB, fb, 0, k0, b_col >> 6);
                             else tma_load_3d_pair(b_dst, &tmB, fb, 0, k0, b_col >> 6);
                         } else if (!p.b_kmajor) {
-                            // B [K, N]: 64-column sub-tiles of 64 k-rows (MN-major).
+                            // B [K, N]: 64-column sub-tiles of 64 k-rows (MN-major); a narrow
+                            // unit loads only its own (through the 2-D map when tmB is 3-D).
+                            const CUtensorMap *mb = p.b_3d ? &tmB2 : &tmB;
 #pragma unroll
                             for (int j = 0; j < L::kBSub; ++j)
-                                if (j < b_sub) load(b_dst + j * (kBK * 128), &tmB, b_col + j * 64, k0);
+                                if (j < b_sub) load(b_dst + j * (kBK * 128), mb, b_col + j * 64, k0);
                         } else {
                             // B stored [N, K]: one box of BN/CG n-rows x 64 k (K-major); a
                             // narrow unit's MMA reads only the first width / CG of them.
@@ -564,22 +569,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned short *bias_s = reinterpret_cast<unsigned short *>(smem + L::kOffBias) + ew * L::kBiasCols;
         constexpr int kBiasPerLane = (L::kBiasCols + 31) / 32;
         unsigned short bias_next[kBiasPerLane];
-        // Loads (into registers) the bias columns this warp needs for unit u.
-        auto fetch_bias = [&](int u) {
+        // First column and width of unit u (the divisions happen here, off the
+        // path between an accumulator's arrival and its read-out).
+        auto unit_cols = [&](int u, int &col_base, int &width) {
             const Unit w = unit_info(u, p, BN);
             int mb, nb;
             tile_coords(w.t, p, mb, nb);
+            col_base = nb * BN + w.col0;
+            width = w.width;
+        };
+        // Loads (into registers) the bias columns this warp needs for a unit.
+        auto fetch_bias = [&](int col_base, int width) {
 #pragma unroll
             for (int k = 0; k < kBiasPerLane; ++k) {
                 const int i = lane + 32 * k;
-                const int col = nb * BN + w.col0 + (part + 2 * (i / CW)) * CW + i % CW;
+                const int col = col_base + (part + 2 * (i / CW)) * CW + i % CW;
                 bias_next[k] = (p.has_bias && i < static_cast<int>(L::kBiasCols) && col < p.N &&
-                                (part + 2 * (i / CW)) * CW < w.width)
+                                (part + 2 * (i / CW)) * CW < width)
                                    ? __ldg(reinterpret_cast<const unsigned short *>(p.bias) + col)
                                    : static_cast<unsigned short>(0);   // +0.0 in fp16 and bf16
             }
         };
-        if (group_id < p.num_units) fetch_bias(group_id);
+        if (group_id < p.num_units) {
+            int cb, wd;
+            unit_cols(group_id, cb, wd);
+            fetch_bias(cb, wd);
+        }
         // Staging swizzle, matching the C tensor map: 16-byte chunk j of row r
         // sits at j ^ (r % 8) for 128-byte rows and j ^ ((r / 2) % 4) for 64-byte rows.
         auto swz = [](int row) { return (CW == 64) ? (row & 7) : ((row >> 1) & 3); };
@@ -597,6 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = w.t, split = w.range;
             int m_blk, n_blk;
             tile_coords(t, p, m_blk, n_blk);
+            const bool has_next = u + num_groups < p.num_units;
+            int next_cb = 0, next_wd = 0;
+            if (has_next) unit_cols(u + num_groups, next_cb, next_wd);
             int ok = 1;
             if (lane == 0) ok = wait_bar<true>(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -622,14 +640,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ra[32], rb[32];
             // The unit's first TMEM load goes out before the bias hand-over,
             // which then hides its latency.
-            if (split < 0 && n_sub > 0) tload(0, ra);
+            if (n_sub > 0) tload(0, ra);
             // Publish this unit's bias strip, then start fetching the next unit's.
             __syncwarp();
 #pragma unroll
             for (int k = 0; k < kBiasPerLane; ++k)
                 if (lane + 32 * k < static_cast<int>(L::kBiasCols)) bias_s[lane + 32 * k] = bias_next[k];
             __syncwarp();
-            if (u + num_groups < p.num_units) fetch_bias(u + num_groups);
+            if (has_next) fetch_bias(next_cb, next_wd);
             TGEMM_EPI_STAMP(1);
             uint32_t packed[CW / 2];
             // + bias and activation for sub-chunk H of a chunk, one rounding into
@@ -719,16 +737,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     release_acc(acc);
                 } else {
                     float *mine = region(split);
-#pragma unroll 1
-                    for (int sub = 0; sub < n_sub; ++sub) {
-                        tload(sub, ra);
-                        tmem_wait_ld(ra);
-                        if (sub == n_sub - 1) release_acc(acc);
+                    // This range's fp32 partials, TMEM loads double-buffered (the first
+                    // one went out at the unit's start).
+                    auto write_partial = [&](int sub, const uint32_t (&r)[32]) {
 #pragma unroll
                         for (int g = 0; g < 8; ++g)
                             __stcg(reinterpret_cast<float4 *>(mine + sub * 1024 + g * 128 + lane * 4),
-                                   make_float4(__uint_as_float(ra[4 * g]), __uint_as_float(ra[4 * g + 1]),
-                                               __uint_as_float(ra[4 * g + 2]), __uint_as_float(ra[4 * g + 3])));
+                                   make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                               __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+                    };
+#pragma unroll 1
+                    for (int sub = 0; sub < n_sub; sub += 2) {
+                        tmem_wait_ld(ra);
+                        if (sub + 1 < n_sub) tload(sub + 1, rb);
+                        else release_acc(acc);
+                        write_partial(sub, ra);
+                        if (sub + 1 >= n_sub) break;
+                        tmem_wait_ld(rb);
+                        if (sub + 2 < n_sub) tload(sub + 2, ra);
+                        else release_acc(acc);
+                        write_partial(sub + 1, rb);
                     }
                     if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(40);
                     __threadfence();

@@ -304,7 +304,7 @@ Cfg choose_config(int64_t M, int64_t N, int64_t K, int num_sms) {
 
 template <int BN, int ST, int CG, int KSUB>
 cudaError_t launch_fused(DeviceInfo *d, int bit, const CUtensorMap &ta, const CUtensorMap &tb,
-                         const CUtensorMap &tc, const KParams &p, int64_t tiles, cudaStream_t s) {
+                         const CUtensorMap &tb2, const CUtensorMap &tc, const KParams &p, int64_t tiles, cudaStream_t s) {
     using L = Smem<BN, ST, CG>;
     auto kernel = tgemm_fused_kernel<BN, ST, CG, KSUB>;
     int max_groups = d->num_sms;
@@ -344,7 +344,7 @@ cudaError_t launch_fused(DeviceInfo *d, int bit, const CUtensorMap &ta, const CU
 #endif
     const int groups = static_cast<int>(std::min<int64_t>(tiles, max_groups));
     if (CG == 1) {
-        kernel<<<groups, kThreads, L::kDynamicBytes, s>>>(ta, tb, tc, p);
+        kernel<<<groups, kThreads, L::kDynamicBytes, s>>>(ta, tb, tb2, tc, p);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t lc;
@@ -360,7 +360,7 @@ cudaError_t launch_fused(DeviceInfo *d, int bit, const CUtensorMap &ta, const CU
     lc.stream = s;
     lc.attrs = la;
     lc.numAttrs = 1;
-    return cudaLaunchKernelEx(&lc, kernel, ta, tb, tc, p);
+    return cudaLaunchKernelEx(&lc, kernel, ta, tb, tb2, tc, p);
 }
 
 // Work units of a plan: split-K pieces, whole tiles, narrow column parts.
@@ -371,7 +371,7 @@ int64_t count_units(int64_t tiles, int split_k, int64_t split_first, int64_t nar
 
 // Fills the tile counts and instruction descriptor for `cfg` and launches.
 cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, const CUtensorMap &tb,
-                          const CUtensorMap &tc, KParams p, cudaStream_t s, bool bf16) {
+                          const CUtensorMap &tb2, const CUtensorMap &tc, KParams p, cudaStream_t s, bool bf16) {
     p.num_m = static_cast<int>(cdiv(p.M, kBM * cfg.cg));
     p.num_n = static_cast<int>(cdiv(p.N, cfg.bn));
     p.num_kb = static_cast<int>(cdiv(p.K, kBK));
@@ -402,18 +402,16 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
     const int narrow_w = cfg.bn / p.narrow_parts;
     p.idesc_narrow = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(narrow_w),
                                p.a_mn != 0, p.b_kmajor == 0);
-    // (A 3-D B box always carries all bn / cg columns.)
-    p.stage_tx_narrow = (p.b_kmajor || p.b_3d)
-                            ? p.stage_tx
-                            : static_cast<uint32_t>(kBM * kBK * 2 + (narrow_w / cfg.cg / 64) * 64 * kBK * 2);
+    p.stage_tx_narrow = p.b_kmajor ? p.stage_tx
+                                   : static_cast<uint32_t>(kBM * kBK * 2 + (narrow_w / cfg.cg / 64) * 64 * kBK * 2);
     switch (cfg.bit) {
-        case 1: return launch_fused<256, 4, 1, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 2: return launch_fused<128, 6, 1, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 4: return launch_fused<64, 8, 1, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 8: return launch_fused<256, 6, 2, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 16: return launch_fused<128, 8, 2, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
-        case 32: return launch_fused<192, 4, 1, 1>(d, cfg.bit, ta, tb, tc, p, units, s);
-        default: return launch_fused<224, 6, 2, 2>(d, cfg.bit, ta, tb, tc, p, units, s);
+        case 1: return launch_fused<256, 4, 1, 1>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
+        case 2: return launch_fused<128, 6, 1, 1>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
+        case 4: return launch_fused<64, 8, 1, 1>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
+        case 8: return launch_fused<256, 6, 2, 2>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
+        case 16: return launch_fused<128, 8, 2, 2>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
+        case 32: return launch_fused<192, 4, 1, 1>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
+        default: return launch_fused<224, 6, 2, 2>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
     }
 }
 
@@ -433,7 +431,7 @@ cudaError_t repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t
 // x 64 n; stored [N, K]: BN/CG n-rows x 64 k.  C: 32 rows x the chunk width.
 bool encode_maps(const Cfg &cfg, const void *a, int64_t lda, int ta, const void *b, int64_t ldb, int tb,
                  void *C, int64_t ldc, bool tma_store, int64_t M, int64_t N, int64_t K, bool bf16,
-                 CUtensorMap *tma, CUtensorMap *tmb, CUtensorMap *tmc, KParams *p) {
+                 CUtensorMap *tma, CUtensorMap *tmb, CUtensorMap *tmb2, CUtensorMap *tmc, KParams *p) {
     const int bcols = cfg.bn / cfg.cg;
     std::memset(tmc, 0, sizeof(*tmc));
     // One 3-D copy per k-block for B [K, N] when every CTA's columns start on a
@@ -448,12 +446,15 @@ bool encode_maps(const Cfg &cfg, const void *a, int64_t lda, int ta, const void 
         (b3d || (tb ? make_map(tmb, b, N, K, ldb, kBK, static_cast<uint32_t>(bcols), bf16)
                     : make_map(tmb, b, K, N, ldb, 64, kBK, bf16))) &&
         (!tma_store || make_map(tmc, C, M, N, ldc, static_cast<uint32_t>(cfg.cw()), 32, bf16));
+    // The 2-D map of B [K, N] for narrow units when tmB is the 3-D view.
+    const bool ok2 = !b3d || make_map(tmb2, b, K, N, ldb, 64, kBK, bf16);
+    if (!b3d) std::memcpy(tmb2, tmb, sizeof(*tmb));
     p->a_mn = ta;
     p->b_kmajor = tb;
     p->b_3d = b3d ? 1 : 0;
     p->stage_tx = static_cast<uint32_t>(kBM * kBK * 2 +
                                         (tb ? bcols * kBK * 2 : cdiv(bcols, 64) * 64 * kBK * 2));
-    return ok;
+    return ok && ok2;
 }
 
 // Work plan: which tiles are cut, and how.
@@ -548,11 +549,11 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
 
     const Cfg cfg = choose_config(M, N, K, d->num_sms);
     const bool tma_store = (ldc % 8) == 0;
-    CUtensorMap tma, tmb, tmc;
+    CUtensorMap tma, tmb, tmb2, tmc;
     KParams p;
     std::memset(&p, 0, sizeof(p));
     if (!encode_maps(cfg, a_use, lda_use, ta, b_use, ldb_use, tb, C, ldc, tma_store, M, N, K, bf16,
-                     &tma, &tmb, &tmc, &p)) {
+                     &tma, &tmb, &tmb2, &tmc, &p)) {
         release();
         return TGEMM_ERR_CUDA;
     }
@@ -592,7 +593,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
         p.partials = static_cast<float *>(scratch_split);
         p.counters = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch_split) + pbytes);
     }
-    const cudaError_t e = launch_config(d, cfg, tma, tmb, tmc, p, stream, bf16);
+    const cudaError_t e = launch_config(d, cfg, tma, tmb, tmb2, tmc, p, stream, bf16);
     release();
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -701,11 +702,11 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
 
     const Cfg cfg = choose_config(M, N, K, d->num_sms);
     const bool tma_store = (ldc % 8) == 0;
-    CUtensorMap tma, tmb, tmc;
+    CUtensorMap tma, tmb, tmb2, tmc;
     KParams p;
     std::memset(&p, 0, sizeof(p));
     if (!encode_maps(cfg, a_use, lda_use, 0, b_use, ldb_use, 0, C, ldc, tma_store, M, N, K, bf16, &tma,
-                     &tmb, &tmc, &p))
+                     &tmb, &tmb2, &tmc, &p))
         return TGEMM_ERR_CUDA;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
@@ -724,7 +725,7 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
         p.narrow_first = static_cast<int>(plan.narrow_first);
         p.narrow_parts = plan.narrow_parts;
     }
-    const cudaError_t e = launch_config(d, cfg, tma, tmb, tmc, p, stream, bf16);
+    const cudaError_t e = launch_config(d, cfg, tma, tmb, tmb2, tmc, p, stream, bf16);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return TGEMM_ERR_CUDA;
