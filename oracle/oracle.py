@@ -21,6 +21,7 @@ EPI_NONE, EPI_RELU, EPI_BIAS, EPI_BIAS_RELU, EPI_GELU, EPI_BIAS_GELU = 0, 1, 2, 
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "attention_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -38,10 +39,10 @@ def dtype_code(name) -> int:
 
 def build(force: bool = False) -> str:
     """Compile liboracle.so with gcc (OpenMP if the compiler supports it)."""
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+    if not force and os.path.exists(_LIB) and all(os.path.getmtime(_LIB) >= os.path.getmtime(f) for f in _SRCS):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp] + _SRCS + ["-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
                        capture_output=True, text=True)
@@ -67,6 +68,9 @@ def _load():
             lib.oracle_decode.argtypes = [p, p, i64, ctypes.c_int]
             lib.oracle_decode.restype = ctypes.c_int
             lib.oracle_max_threads.restype = ctypes.c_int
+            lib.oracle_attention_f64.argtypes = [p, p, p, p, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                                 p, i64, ctypes.c_int]
+            lib.oracle_attention_f64.restype = ctypes.c_int
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
@@ -138,3 +142,32 @@ def max_threads() -> int:
 
 def set_threads(n: int) -> None:
     _load().oracle_set_threads(int(n))
+
+
+def attention_f64(Q, K, V, B: int, S: int, H: int, D: int, causal: bool, dtype: int, rows=None,
+                  abs_v: bool = False) -> np.ndarray:
+    """Unrounded fp64 attention output of "TileLang で GPU カーネル設計を解説" §6.
+
+    Q, K, V: uint16 bit patterns [B, S, H, D] (any shape with that many
+    elements, row-major).  Returns float64 [B*S*H, D] (every row, in [B, S, H]
+    order) or [len(rows), D] for rows given as flat (b * S + i) * H + h.  With
+    abs_v, |V| replaces V (the magnitude sum_j w_ij |V_j|).
+    """
+    lib = _load()
+    q = np.ascontiguousarray(_u16(Q)).reshape(-1)
+    k = np.ascontiguousarray(_u16(K)).reshape(-1)
+    v = np.ascontiguousarray(_u16(V)).reshape(-1)
+    if not (q.size == k.size == v.size == B * S * H * D):
+        raise ValueError("Q, K, V must each hold B*S*H*D elements")
+    rows_arr = None
+    nrows = B * S * H
+    if rows is not None:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        nrows = rows_arr.shape[0]
+    out = np.empty((nrows, D), dtype=np.float64)
+    rc = lib.oracle_attention_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, S, H, D, int(bool(causal)),
+                                  int(bool(abs_v)), _ptr(rows_arr) if rows_arr is not None else None, nrows,
+                                  int(dtype))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return out
