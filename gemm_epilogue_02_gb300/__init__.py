@@ -12,7 +12,8 @@ from ._binding import (  # noqa: F401
     TGEMM_BF16, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_GELU, TGEMM_EPI_BIAS_RELU, TGEMM_EPI_GELU,
     TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_F16,
     EXPORTED, NOALLOC_SCRATCH_BYTES, PLAN_FIELDS, STATUS, TgemmError, library_path, load,
-    tgemm_last_device_status, tgemm_plan, tgemm_run, tgemm_run_ex, tgemm_run_host, tgemm_run_noalloc,
+    tgemm_attention_fwd, tgemm_last_device_status, tgemm_plan, tgemm_run, tgemm_run_ex, tgemm_run_host,
+    tgemm_run_noalloc,
     tgemm_status_string, tgemm_version,
 )
 from .build import build  # noqa: F401
@@ -83,3 +84,26 @@ def run_host(A: torch.Tensor, B: torch.Tensor, bias, C: torch.Tensor, epilogue="
     if st != 0:
         raise TgemmError(st, "tgemm_run_host")
     return C
+
+
+def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, causal: bool = False,
+              stream=None) -> torch.Tensor:
+    """O = softmax(Q K^T / sqrt(dim)) V (causal: keys up to the query) on CUDA
+    tensors of shape [batch, seq, heads, 64], contiguous, float16 or bfloat16,
+    enqueued on the current (or given) stream.  Raises TgemmError on a status
+    other than TGEMM_OK."""
+    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O)):
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [batch, seq, heads, dim] tensor")
+    if not (Q.shape == K.shape == V.shape == O.shape):
+        raise ValueError("Q, K, V and O must have one shape")
+    if not (Q.dtype == K.dtype == V.dtype == O.dtype) or Q.dtype not in _DT:
+        raise ValueError("Q, K, V and O must share dtype float16 or bfloat16")
+    batch, seq, heads, dim = Q.shape
+    s = stream if stream is not None else torch.cuda.current_stream(Q.device)
+    with torch.cuda.device(Q.device):
+        st = tgemm_attention_fwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), batch, seq, heads, dim,
+                                 int(causal), _DT[Q.dtype], s.cuda_stream)
+    if st != 0:
+        raise TgemmError(st, "tgemm_attention_fwd")
+    return O

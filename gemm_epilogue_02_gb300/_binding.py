@@ -19,7 +19,8 @@ STATUS = {0: "TGEMM_OK", 1: "TGEMM_ERR_INVALID_ARG", 2: "TGEMM_ERR_ALIGNMENT",
           3: "TGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TGEMM_ERR_ALIAS", 5: "TGEMM_ERR_CUDA",
           6: "TGEMM_ERR_TIMEOUT", 7: "TGEMM_ERR_SCRATCH_LIMIT"}
 EXPORTED = ("tgemm_run", "tgemm_run_ex", "tgemm_run_host", "tgemm_status_string",
-            "tgemm_last_device_status", "tgemm_version", "tgemm_run_noalloc", "tgemm_plan")
+            "tgemm_last_device_status", "tgemm_version", "tgemm_run_noalloc", "tgemm_plan",
+            "tgemm_attention_fwd")
 PLAN_FIELDS = ("bn", "cg", "stages", "tiles", "groups", "split_k", "split_first", "narrow_first",
                "narrow_parts", "units")
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -64,6 +65,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.tgemm_version.restype = i32
         lib.tgemm_plan.argtypes = [i64, i64, i64, i32, p]
         lib.tgemm_plan.restype = i32
+        lib.tgemm_attention_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, i32, i32, p]
+        lib.tgemm_attention_fwd.restype = i32
         _lib = lib
         return lib
 
@@ -121,3 +124,8 @@ def tgemm_plan(M: int, N: int, K: int, num_sms: int) -> dict:
     if st != 0:
         raise TgemmError(st, "tgemm_plan")
     return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+
+
+def tgemm_attention_fwd(Q: int, K: int, V: int, O: int, batch: int, seq: int, heads: int, dim: int,
+                        causal: int, dtype: int, stream: int = 0) -> int:
+    return int(load().tgemm_attention_fwd(Q, K, V, O, batch, seq, heads, dim, int(causal), dtype, stream))

@@ -1,0 +1,329 @@
+// Attention forward pass (the output of FlashAttention) on tcgen05:
+//
+//     O[b, i, h, :] = sum_j softmax_j(scale * Q[b, i, h, :] . K[b, j, h, :]) V[b, j, h, :]
+//
+// over all keys j < S, or j <= i when causal, scale = 1 / sqrt(dim), tensors
+// [batch, seq, heads, dim] with dim contiguous: the computation of
+// "TileLang で GPU カーネル設計を解説" §6 (two chained GEMMs with an online
+// softmax: running row maximum and row sum, the accumulator rescaled when the
+// maximum grows, P rounded to the input format before the second GEMM, the
+// sum of unrounded P as the final divisor), laid out for sm_103a.
+//
+// A CTA owns 128 query rows of one (batch, head); dim = 64; keys go in
+// blocks of 128:
+//
+//   warp 0      TMA producer: the Q tile once, then K and V tiles [128 x 64]
+//               into a 3-stage ring (one full / empty barrier per stage).
+//   warp 1      allocates TMEM (two 128-column score accumulators, a 64-column
+//               output accumulator); one lane issues S_j = Q K_j^T (M = 128,
+//               N = 128, both operands K-major) into score buffer j % 2, then
+//               O += P_{j-1} V_{j-1} (P from shared memory, K-major; V
+//               MN-major, N = 64) once the softmax has published P_{j-1}.
+//   warps 4..7  softmax, one thread per query row (TMEM lane): read the row's
+//               128 scores, mask keys past the sequence (and after the query
+//               when causal), new running maximum, exp2 of the scaled scores,
+//               row sum; after the previous P.V has completed: write P (16-bit,
+//               128B-swizzled, two 64-key sub-tiles) and rescale the O row in
+//               TMEM by exp2(m_old - m_new); at the end divide by the row sum,
+//               round, store.
+//
+// Every barrier wait is bounded as in the GEMM kernel; on expiry the CTA
+// records TGEMM_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include "gemm_kernel.cuh"
+
+namespace tgemm {
+
+constexpr int kAttnBM = 128;          // query rows per CTA
+constexpr int kAttnBN = 128;          // keys per block
+constexpr int kAttnD = 64;            // head dimension
+constexpr int kAttnStages = 3;        // K/V ring depth
+constexpr int kAttnThreads = 256;     // warp 0 producer, warp 1 MMA, warps 4..7 softmax
+
+struct AttnParams {
+    int B, S, H;
+    float scale_log2;                 // log2(e) / sqrt(dim)
+    void *O;
+    unsigned int *status;
+};
+
+struct AttnSmem {
+    static constexpr uint32_t kTile = kAttnBN * kAttnD * 2;          // 16 KiB: a [128 x 64] 16-bit tile
+    static constexpr uint32_t kQ = 0;
+    static constexpr uint32_t kKV = kQ + kTile;                       // stage s: K, then V
+    static constexpr uint32_t kP = kKV + kAttnStages * 2 * kTile;     // P: keys 0-63, then 64-127
+    static constexpr uint32_t kBar = kP + 2 * kTile;
+    // q_full, kv_full[3], kv_empty[3], s_full[2], s_empty[2], p_full, pv_done, drain
+    static constexpr uint32_t kNumBars = 14;
+    static constexpr uint32_t kHolder = kBar + kNumBars * 8;
+    static constexpr uint32_t kAbort = kHolder + 4;
+    static constexpr uint32_t kBytes = kAbort + 4;
+    static constexpr uint32_t kTmemCols = 512;                        // S0 at 0, S1 at 128, O at 256
+    static_assert(kKV % 1024 == 0 && kP % 1024 == 0, "swizzled tiles need 1 KiB alignment");
+    static_assert(kBytes <= 232448, "shared memory budget");
+};
+
+template <bool kBf16, bool kCausal>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    using L = AttnSmem;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
+    const uint32_t sbase = smem_u32(smem);
+    if (sbase & 1023u) {
+        if (threadIdx.x == 0) atomicExch(p.status, kStatusLaunch);
+        return;
+    }
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * kAttnBM;
+    const int nkb = (p.S + kAttnBN - 1) / kAttnBN;
+    const int nblk = kCausal ? min(nkb, qt + 1) : nkb;     // blocks of equal size: the diagonal is block qt
+    const uint32_t bar0 = sbase + L::kBar;
+    const uint32_t q_full = bar0;
+    auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bar0 + 8u * (4 + s); };
+    auto s_full = [&](int x) { return bar0 + 8u * (7 + x); };
+    auto s_empty = [&](int x) { return bar0 + 8u * (9 + x); };
+    const uint32_t p_full = bar0 + 8u * 11;
+    const uint32_t pv_done = bar0 + 8u * 12;
+    const uint32_t drain_bar = bar0 + 8u * 13;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kHolder);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kAttnStages; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(s_full(x), 1);
+            mbar_init(s_empty(x), 4);          // the four softmax warps
+        }
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_shared();
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(smem_u32(tmem_holder), L::kTmemCols);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            mbar_arrive_expect_tx(q_full, L::kTile);
+            tma_load_4d(sbase + L::kQ, &tmQ, q_full, 0, h, q0, b);
+            uint32_t uses[kAttnStages] = {0, 0, 0};
+            bool ok = true;
+            for (int j = 0; j < nblk; ++j) {
+                const int s = j % kAttnStages;
+                const uint32_t ph = static_cast<uint32_t>(j / kAttnStages) & 1u;
+                if (!wait_bar<true>(kv_empty(s), ph ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                mbar_arrive_expect_tx(kv_full(s), 2 * L::kTile);
+                const uint32_t kdst = sbase + L::kKV + s * 2 * L::kTile;
+                tma_load_4d(kdst, &tmK, kv_full(s), 0, h, j * kAttnBN, b);
+                tma_load_4d(kdst + L::kTile, &tmV, kv_full(s), 0, h, j * kAttnBN, b);
+                ++uses[s];
+            }
+            if (!ok) {
+                // Let every copy this thread started land before the CTA exits.
+                drain_wait(q_full, 0);
+                for (int s = 0; s < kAttnStages; ++s)
+                    if (uses[s]) drain_wait(kv_full(s), (uses[s] - 1u) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16(kBf16, kAttnBM, kAttnBN, false, false);
+            const uint32_t idesc_o = idesc_f16(kBf16, kAttnBM, kAttnD, false, true);
+            // K-major tiles: 8-row groups 1 KiB apart, +32 B per 16-wide k step.
+            // V (MN-major, one 64-column sub-tile): +2 KiB per 16 keys.
+            // P: two 64-key K-major sub-tiles 16 KiB apart.
+            const uint64_t q_desc = sw128_desc(sbase + L::kQ, 16, 1024);
+            const uint64_t p_desc = sw128_desc(sbase + L::kP, 16, 1024);
+            bool ok = wait_bar<false>(q_full, 0, abort_flag, p.status);
+            for (int j = 0; ok && j <= nblk; ++j) {
+                if (j < nblk) {
+                    const int s = j % kAttnStages;
+                    const int x = j & 1;
+                    if (!wait_bar<false>(kv_full(s), static_cast<uint32_t>(j / kAttnStages) & 1u, abort_flag,
+                                         p.status) ||
+                        !wait_bar<true>(s_empty(x), (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag,
+                                        p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t k_desc = sw128_desc(sbase + L::kKV + s * 2 * L::kTile, 16, 1024);
+                    const uint32_t d_s = tmem_base + static_cast<uint32_t>(x * kAttnBN);
+#pragma unroll
+                    for (int k = 0; k < kAttnD / kUmmaK; ++k)
+                        mma_f16_ss<1>(d_s, q_desc + k * 2, k_desc + k * 2, idesc_s, k > 0 ? 1u : 0u);
+                    mma_commit<1>(s_full(x));
+                }
+                if (j >= 1) {
+                    const int jp = j - 1;
+                    const int sp = jp % kAttnStages;
+                    if (!wait_bar<false>(p_full, static_cast<uint32_t>(jp) & 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t v_desc =
+                        sw128_desc(sbase + L::kKV + sp * 2 * L::kTile + L::kTile, kBK * 128, 1024);
+#pragma unroll
+                    for (int k = 0; k < kAttnBN / kUmmaK; ++k)
+                        mma_f16_ss<1>(tmem_base + 2 * kAttnBN,
+                                      p_desc + static_cast<uint32_t>(k >> 2) * (L::kTile >> 4) + (k & 3) * 2,
+                                      v_desc + static_cast<uint32_t>(k) * (2048 >> 4), idesc_o,
+                                      (jp > 0 || k > 0) ? 1u : 0u);
+                    mma_commit<1>(kv_empty(sp));
+                    mma_commit<1>(pv_done);
+                }
+            }
+            // All MMAs issued by this thread complete before TMEM is released.
+            mma_commit_local<1>(drain_bar);
+            drain_wait(drain_bar, 0);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int query = q0 + row;
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        float m = -INFINITY;      // running maximum of scale*log2(e)*score
+        float l = 0.0f;           // running sum of exp2(t - m)
+        bool ok = true;
+        auto wait_all = [&](uint32_t bar, uint32_t parity) {
+            int w = 1;
+            if (lane == 0) w = wait_bar<true>(bar, parity, abort_flag, p.status) ? 1 : 0;
+            return __shfl_sync(0xffffffffu, w, 0) != 0;
+        };
+        for (int j = 0; j < nblk; ++j) {
+            const int x = j & 1;
+            if (!wait_all(s_full(x), static_cast<uint32_t>(j >> 1) & 1u)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(x * kAttnBN + 32 * c), sr[c]);
+            tmem_wait_ld(sr[0]);
+            tmem_wait_ld(sr[1]);
+            tmem_wait_ld(sr[2]);
+            tmem_wait_ld(sr[3]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty(x));
+            // Scaled scores (log2 domain), masked keys at -inf, the block maximum.
+            const int key0 = j * kAttnBN;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int key = key0 + 32 * c + i;
+                    float t = __uint_as_float(sr[c][i]) * p.scale_log2;
+                    if (key >= p.S || (kCausal && key > query)) t = -INFINITY;
+                    sr[c][i] = __float_as_uint(t);
+                    mx = fmaxf(mx, t);
+                }
+            const float m_new = fmaxf(m, mx);
+            const float m_sub = (m_new == -INFINITY) ? 0.0f : m_new;
+            const float alpha = exp2f(m - m_sub);          // 0 on the first block (m = -inf)
+            float rowsum = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float pv = exp2f(__uint_as_float(sr[c][i]) - m_sub);
+                    rowsum += pv;
+                    sr[c][i] = __float_as_uint(pv);
+                }
+            l = l * alpha + rowsum;
+            m = m_new;
+            // P's buffer and the O accumulator are free once the previous P.V is done.
+            if (j >= 1 && !wait_all(pv_done, static_cast<uint32_t>(j - 1) & 1u)) { ok = false; break; }
+            tc_fence_after();
+            // P row, 16-bit, 128B-swizzled: keys 64*t + 8*ch .. +8 of this row go to
+            // 16-byte chunk ch ^ (row % 8) of row `row` in sub-tile t.
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const int c = (64 * t + 8 * ch) / 32, i0 = (64 * t + 8 * ch) % 32;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = pack2<kBf16>(__uint_as_float(sr[c][i0 + 2 * e]), __uint_as_float(sr[c][i0 + 2 * e + 1]));
+                    const uint32_t addr = sbase + L::kP + t * L::kTile + row * 128 + ((ch ^ (row & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                                 "r"(w[2]), "r"(w[3])
+                                 : "memory");
+                }
+            if (j >= 1) {
+                // O row *= exp2(m_old - m_new), in TMEM.
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t o[32];
+                    const uint32_t ta = lane_base + static_cast<uint32_t>(2 * kAttnBN + 32 * c);
+                    tmem_ld_32x32b_x32(ta, o);
+                    tmem_wait_ld(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st_32x32b_x32(ta, o);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_shared();            // P visible to the tensor core
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok && wait_all(pv_done, static_cast<uint32_t>(nblk - 1) & 1u)) {
+            tc_fence_after();
+            uint32_t o[2][32];
+            tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(2 * kAttnBN), o[0]);
+            tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(2 * kAttnBN + 32), o[1]);
+            tmem_wait_ld(o[0]);
+            tmem_wait_ld(o[1]);
+            if (query < p.S) {
+                const float inv = 1.0f / l;
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<unsigned short *>(p.O) +
+                                                       ((static_cast<long long>(b) * p.S + query) * p.H + h) * kAttnD);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int c = q / 4, i0 = (q % 4) * 8;
+                    uint4 v;
+                    v.x = pack2<kBf16>(__uint_as_float(o[c][i0 + 0]) * inv, __uint_as_float(o[c][i0 + 1]) * inv);
+                    v.y = pack2<kBf16>(__uint_as_float(o[c][i0 + 2]) * inv, __uint_as_float(o[c][i0 + 3]) * inv);
+                    v.z = pack2<kBf16>(__uint_as_float(o[c][i0 + 4]) * inv, __uint_as_float(o[c][i0 + 5]) * inv);
+                    v.w = pack2<kBf16>(__uint_as_float(o[c][i0 + 6]) * inv, __uint_as_float(o[c][i0 + 7]) * inv);
+                    dst[q] = v;
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc<1>(tmem_base, L::kTmemCols);
+}
+
+}  // namespace tgemm

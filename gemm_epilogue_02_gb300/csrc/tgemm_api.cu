@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
@@ -17,6 +18,7 @@
 #include "../../include/tgemm.h"
 #include "aux_kernels.cuh"
 #include "gemm_kernel.cuh"
+#include "attn_kernel.cuh"
 
 namespace tgemm {
 namespace {
@@ -34,6 +36,7 @@ struct DeviceInfo {
     cudaMemPool_t pool = nullptr;
     std::mutex mu;          // guards lazily set kernel attributes
     unsigned attr_set = 0;  // bit per kernel configuration
+    unsigned attn_attr_set = 0;   // bit per attention kernel (format x causal)
     int max_clusters[3] = {0, 0, 0};   // co-resident clusters per CTA-group size
     cudaStream_t copy_in = nullptr;    // tgemm_run_host: host->device copies
     cudaStream_t copy_out = nullptr;   // tgemm_run_host: device->host copies
@@ -779,6 +782,98 @@ extern "C" tgemm_status tgemm_run_ex(const void *A, const void *B, const void *b
         return TGEMM_ERR_INVALID_ARG;
     return run_device(d, A, B, bias, C, M, N, K, lda, ldb, ldc, dtype, epilogue,
                       reinterpret_cast<cudaStream_t>(stream), transpose_a, transpose_b);
+}
+
+namespace tgemm {
+namespace {
+
+// One head's rows of a [batch, seq, heads, 64] tensor: the 4-D view (dim,
+// heads, seq, batch) with boxes of 64 x 1 x 128 x 1 (a [128 x 64] tile,
+// 128-byte swizzled); rows past seq read as zero.
+bool make_map_bshd(CUtensorMap *m, const void *base, int64_t B, int64_t S, int64_t H, bool bf16) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kAttnD), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kAttnD * 2), static_cast<cuuint64_t>(H * kAttnD * 2),
+                                   static_cast<cuuint64_t>(S * H * kAttnD * 2)};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(kAttnD), 1, static_cast<cuuint32_t>(kAttnBM), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool kBf16, bool kCausal>
+cudaError_t launch_attention(DeviceInfo *d, unsigned bit, const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv, const AttnParams &p, cudaStream_t s) {
+    auto kernel = attn_fwd_kernel<kBf16, kCausal>;
+    {
+        std::lock_guard<std::mutex> g(d->mu);
+        if (!(d->attn_attr_set & bit)) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnSmem::kBytes);
+            if (e != cudaSuccess) return e;
+            d->attn_attr_set |= bit;
+        }
+    }
+    const dim3 grid(static_cast<unsigned>(cdiv(p.S, kAttnBM)), static_cast<unsigned>(p.H),
+                    static_cast<unsigned>(p.B));
+    kernel<<<grid, kAttnThreads, AttnSmem::kBytes, s>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace tgemm
+
+extern "C" tgemm_status tgemm_attention_fwd(const void *Q, const void *K, const void *V, void *O, int64_t batch,
+                                            int64_t seq, int64_t heads, int64_t dim, int causal,
+                                            tgemm_dtype dtype, tgemm_stream_t stream) {
+    if (batch < 0 || seq < 0 || heads < 0 || dim != kAttnD || (causal != 0 && causal != 1) ||
+        (dtype != TGEMM_F16 && dtype != TGEMM_BF16))
+        return TGEMM_ERR_INVALID_ARG;
+    if (batch > 65535 || heads > 65535 || seq > (int64_t(1) << 30) || batch * seq * heads > (int64_t(1) << 31))
+        return TGEMM_ERR_INVALID_ARG;
+    if (batch == 0 || seq == 0 || heads == 0) return TGEMM_OK;
+    if (!Q || !K || !V || !O) return TGEMM_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return TGEMM_ERR_ALIGNMENT;
+    const int64_t rows = batch * seq * heads;
+    const Range ro = span(O, rows, dim, dim);
+    if (overlaps(ro, span(Q, rows, dim, dim)) || overlaps(ro, span(K, rows, dim, dim)) ||
+        overlaps(ro, span(V, rows, dim, dim)))
+        return TGEMM_ERR_ALIAS;
+    DeviceInfo *d = nullptr;
+    tgemm_status st = current_device(&d);
+    if (st != TGEMM_OK) return st;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!is_device_memory(Q, dev) || !is_device_memory(K, dev) || !is_device_memory(V, dev) ||
+        !is_device_memory(O, dev))
+        return TGEMM_ERR_INVALID_ARG;
+    const bool bf16 = dtype == TGEMM_BF16;
+    CUtensorMap tq, tk, tv;
+    if (!make_map_bshd(&tq, Q, batch, seq, heads, bf16) || !make_map_bshd(&tk, K, batch, seq, heads, bf16) ||
+        !make_map_bshd(&tv, V, batch, seq, heads, bf16))
+        return TGEMM_ERR_CUDA;
+    AttnParams p;
+    p.B = static_cast<int>(batch);
+    p.S = static_cast<int>(seq);
+    p.H = static_cast<int>(heads);
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dim)));
+    p.O = O;
+    p.status = d->status;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (bf16) e = causal ? launch_attention<true, true>(d, 1u, tq, tk, tv, p, s)
+                         : launch_attention<true, false>(d, 2u, tq, tk, tv, p, s);
+    else e = causal ? launch_attention<false, true>(d, 4u, tq, tk, tv, p, s)
+                    : launch_attention<false, false>(d, 8u, tq, tk, tv, p, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return TGEMM_ERR_CUDA;
+    }
+    return TGEMM_OK;
 }
 
 extern "C" tgemm_status tgemm_run(const void *A, const void *B, const void *bias, void *C,

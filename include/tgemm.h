@@ -207,6 +207,36 @@ tgemm_status tgemm_last_device_status(void);
 int tgemm_version(void);
 
 /*
+ * tgemm_attention_fwd — enqueue the attention forward pass (the output of
+ * FlashAttention, "TileLang で GPU カーネル設計を解説" §6) on `stream`:
+ *
+ *   O[b, i, h, :] = sum_j softmax_j(scale * Q[b, i, h, :] . K[b, j, h, :]) V[b, j, h, :],
+ *   scale = 1 / sqrt(dim),
+ *
+ * over all keys j < seq, or only j <= i when causal = 1.
+ *
+ * Arguments: Q, K, V, O device pointers in `dtype` (fp16 or bf16), each a
+ * dense [batch, seq, heads, dim] array (dim contiguous, then heads, then seq,
+ * then batch), 16-byte aligned; O must not overlap Q, K or V.  dim must be 64.
+ * Ownership stays with the caller; the call only reads Q, K, V and writes O.
+ *
+ * Arithmetic: scores and P.V products accumulate in fp32; the softmax runs
+ * blockwise over 128 keys at a time with a running maximum and sum (the
+ * online softmax), P is rounded to `dtype` before it multiplies V, and each
+ * output row is divided by the fp32 sum of the unrounded P and rounded once
+ * to `dtype` (round-to-nearest-even).
+ *
+ * Returns TGEMM_ERR_INVALID_ARG (negative sizes, dim != 64, causal not 0/1,
+ * bad dtype, batch or heads above 65535, a NULL or host pointer for a
+ * non-empty problem), TGEMM_ERR_ALIGNMENT, TGEMM_ERR_ALIAS,
+ * TGEMM_ERR_UNSUPPORTED_DEVICE, TGEMM_ERR_CUDA; TGEMM_OK once enqueued.
+ * An empty problem (batch, seq or heads 0) enqueues nothing.
+ */
+tgemm_status tgemm_attention_fwd(const void *Q, const void *K, const void *V, void *O,
+                                 int64_t batch, int64_t seq, int64_t heads, int64_t dim,
+                                 int causal, tgemm_dtype dtype, tgemm_stream_t stream);
+
+/*
  * tgemm_plan — the work plan tgemm_run (and tgemm_run_ex / tgemm_run_host per
  * chunk) uses for an M x N x K problem on a GPU with num_sms SMs.  Host logic
  * only: no device is touched, so it also answers on a machine without a GPU.

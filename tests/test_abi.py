@@ -100,3 +100,26 @@ def test_transposed_layout_validation():
     assert call_ex(0, -1, lda=48, ldb=32) == INVALID
     assert call_ex(1, 1) in (OK, UNSUPPORTED)
     assert call_ex(0, 0, lda=48, ldb=32) in (OK, UNSUPPORTED)
+
+
+def call_attn(**kw):
+    args = dict(Q=0x100000, K=0x200000, V=0x300000, O=0x400000, B=2, S=128, H=2, D=64, causal=0, dtype=0)
+    args.update(kw)
+    return tg.tgemm_attention_fwd(args["Q"], args["K"], args["V"], args["O"], args["B"], args["S"], args["H"],
+                                  args["D"], args["causal"], args["dtype"], 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=128), INVALID), (dict(D=32), INVALID), (dict(B=-1), INVALID), (dict(S=-1), INVALID),
+    (dict(H=-1), INVALID), (dict(causal=2), INVALID), (dict(dtype=2), INVALID), (dict(H=70000), INVALID),
+    (dict(Q=0), INVALID), (dict(O=0), INVALID), (dict(K=0x200008), ALIGN), (dict(O=0x400002), ALIGN),
+    (dict(O=0x300000 + 1024), ALIAS), (dict(O=0x100000), ALIAS),
+])
+def test_attention_arguments_rejected_before_any_launch(kw, code):
+    assert call_attn(**kw) == code
+
+
+def test_attention_empty_problems_and_valid_call():
+    assert call_attn(B=0, Q=0, K=0, V=0, O=0) == OK
+    assert call_attn(S=0) == OK
+    assert call_attn() in (OK, UNSUPPORTED, INVALID)   # no GPU here (or host pointers on one)
