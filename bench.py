@@ -32,6 +32,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import seeded_inputs as si  # noqa: E402
@@ -252,6 +253,142 @@ def run_reference(args, world, rank):
     return 0
 
 
+METRIC_ATTN = "attention forward TFLOP/s (4*B*H*S^2*D, half when causal) on 1 GB300; % of dense fp16 tensor peak"
+
+
+def attn_config(w):
+    return {"workload": w.name, "batch": w.B, "seq_len": w.S, "heads": w.H, "head_dim": w.D, "dtype": w.dtype,
+            "causal": w.causal, "layout": "[batch, seq, heads, dim]", "inputs": "Q, K, V ~N(0,1)", "seed": w.seed,
+            "l2": "flushed between steps (256 MiB write, outside the timed launch)"}
+
+
+def attn_oracle_rows(w, q, k, v, nrows):
+    import oracle
+    total = w.B * w.S * w.H
+    rows = [int(r) for r in (np.arange(nrows) * (total // max(nrows, 1))) % total]
+    b = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.attention_f64(b(q), b(k), b(v), w.B, w.S, w.H, w.D, w.causal, oracle.dtype_code(w.dtype), rows=rows)
+    return time.perf_counter() - t0, rows
+
+
+def attn_cpu_sample(w, q, k, v, target_s):
+    """The fp64 attention oracle on a bounded, spread sample of query rows,
+    growing until one run takes about target_s seconds."""
+    import oracle
+    total = w.B * w.S * w.H
+    n = min(total, 256)
+    while True:
+        t, rows = attn_oracle_rows(w, q, k, v, n)
+        if t >= 0.5 * target_s or n >= total:
+            break
+        n = int(min(total, max(2 * n, n * target_s / max(t, 1e-6))))
+    per_row = 4.0 * w.S * w.D * (0.5 if w.causal else 1.0)   # average flops of one query row
+    return {"value": per_row * len(rows) / t / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": round(t, 3),
+            "sample": f"{len(rows)} of {total} query rows of {w.name} (spread over batch, heads, positions), fp64"}
+
+
+def run_attention_bench(args, world, rank, local):
+    import gemm_epilogue_02_gb300 as tg
+    tg.load()
+    w = si.ATTN_WORKLOADS[args.config]
+    dev = torch.device("cuda", local)
+    q, k, v = si.make_attention_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    od = torch.empty_like(qd)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        tg.attention(qd, kd, vd, od, causal=w.causal, stream=stream)
+
+    launch_ms, t_wall, clk = timed_steps(step, flush, args, dev, stream, world, local)
+    mean_ms, launch_stats = launch_summary(launch_ms, t_wall, args.steps)
+    mean_ms_max = max_over_ranks(mean_ms, world)
+    value = world * w.flops / (mean_ms_max * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        oh = torch.empty_like(qh).pin_memory()
+
+        def host_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            tg.attention(qd, kd, vd, od, causal=w.causal, stream=stream)
+            oh.copy_(od, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup)):
+                host_step()
+            torch.cuda.synchronize(dev)
+            n_e2e = max(3, min(args.steps, 50))
+            es = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+            ee = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+            barrier(world)
+            for i in range(n_e2e):
+                es[i].record(stream)
+                host_step()
+                ee[i].record(stream)
+            torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(es, ee)) / n_e2e, world)
+        e2e = {"value": world * w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 3 * qh.numel() * 2, "d2h_bytes_per_step": oh.numel() * 2,
+               "ms_per_step": e2e_ms, "steps": n_e2e, "host_memory": "pinned"}
+
+    status = tg.tgemm_last_device_status()
+    if rank != 0:
+        return 0 if status == 0 else 1
+    peak, hbm, peak_kind = measured_peaks()
+    achieved = w.flops / (mean_ms * 1e-3) / 1e12
+    line = {"metric": METRIC_ATTN, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup_done, "ms_per_step": mean_ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "config": attn_config(w),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": recorded_traffic(args.config),
+                         "peak_source": f"{peak_kind} dense bf16 burst (fp16 nominal rate is equal)",
+                         "kernel": "attn_fwd_kernel", "algorithmic_flops_per_launch": w.flops,
+                         "algorithmic_bytes_per_launch": 4 * w.B * w.S * w.H * w.D * 2},
+            "clocks": clk.summary(), "gpu_launches": args.steps, "launch_us": launch_stats,
+            "device_status": tg.tgemm_status_string(status), "wall_s_timed_region": t_wall}
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = attn_cpu_sample(w, q, k, v, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0 if status == 0 else 1
+
+
+def run_attention_reference(args, world, rank):
+    """Reference arm for the attention workloads: the fp64 oracle on a bounded
+    row sample per step (rank 0 only)."""
+    if rank != 0:
+        return 0
+    import oracle
+    w = si.ATTN_WORKLOADS[args.config]
+    q, k, v = si.make_attention_inputs(w)
+    nrows = max(1, args.ref_rows)
+    for _ in range(args.warmup):
+        attn_oracle_rows(w, q, k, v, nrows)
+    times = [attn_oracle_rows(w, q, k, v, nrows)[0] for _ in range(args.steps)]
+    t = sum(times) / len(times)
+    per_row = 4.0 * w.S * w.D * (0.5 if w.causal else 1.0)
+    value = per_row * nrows / t / 1e12
+    sample = f"{nrows} of {w.B * w.S * w.H} query rows of {w.name} per step, fp64"
+    line = {"impl": "reference", "metric": METRIC_ATTN, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": attn_config(w),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def workload_config(w):
     return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype": w.dtype,
             "epilogue": w.epilogue, "lda": w.lda or w.K, "ldb": w.ldb or w.N, "ldc": w.ldc or w.N,
@@ -261,28 +398,11 @@ def workload_config(w):
             "l2": "flushed between steps (256 MiB write, outside the timed launch)"}
 
 
-def run_tgemm_bench(args, world, rank, local):
-    import gemm_epilogue_02_gb300 as tg
-    tg.load()
-    w = si.WORKLOADS[args.config]
-    dev = torch.device("cuda", local)
-    A, B, bias = si.make_workload(w)
-    ldc = w.ldc or w.N
-    Ad = A.to(dev)[:, : w.K]
-    Bd = B.to(dev)[:, : w.N]
-    bd = bias.to(dev) if bias is not None else None
-    Cfull = torch.empty((w.M, ldc), dtype=A.dtype, device=dev)
-    Cd = Cfull[:, : w.N]
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.Stream(dev)
-    flops = float(w.flops)
-
-    def step():
-        tg.run(Ad, Bd, bd, Cd, w.epilogue, stream=stream)
-
+def timed_steps(step, flush, args, dev, stream, world, local):
+    """Warm-up (at least W steps and args.soak seconds), then args.steps timed
+    steps bracketed by barriers, each launch timed with CUDA events on `stream`
+    and L2 flushed before it.  Returns (launch ms list, wall seconds, clocks)."""
     with torch.cuda.stream(stream), ClockSampler(local) as clk:
-        # Warm-up: at least W steps and at least args.soak seconds of them, so
-        # clocks and power settle before the timed region.
         t_soak = time.perf_counter()
         done = 0
         while done < args.warmup or time.perf_counter() - t_soak < args.soak:
@@ -308,12 +428,38 @@ def run_tgemm_bench(args, world, rank, local):
         t_wall = time.perf_counter() - t_wall
         clk.mark_end()
         barrier(world)
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    mean_ms = sum(launch_ms) / len(launch_ms)
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], t_wall, clk
+
+
+def launch_summary(launch_ms, t_wall, steps):
     srt = sorted(launch_ms)
     pct = lambda f: srt[min(len(srt) - 1, int(f * len(srt)))] * 1e3
-    launch_stats = {"mean": mean_ms * 1e3, "p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9),
-                    "max": srt[-1] * 1e3, "wall_per_step": t_wall / args.steps * 1e6}
+    mean_ms = sum(launch_ms) / len(launch_ms)
+    return mean_ms, {"mean": mean_ms * 1e3, "p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9),
+                     "max": srt[-1] * 1e3, "wall_per_step": t_wall / steps * 1e6}
+
+
+def run_tgemm_bench(args, world, rank, local):
+    import gemm_epilogue_02_gb300 as tg
+    tg.load()
+    w = si.WORKLOADS[args.config]
+    dev = torch.device("cuda", local)
+    A, B, bias = si.make_workload(w)
+    ldc = w.ldc or w.N
+    Ad = A.to(dev)[:, : w.K]
+    Bd = B.to(dev)[:, : w.N]
+    bd = bias.to(dev) if bias is not None else None
+    Cfull = torch.empty((w.M, ldc), dtype=A.dtype, device=dev)
+    Cd = Cfull[:, : w.N]
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    flops = float(w.flops)
+
+    def step():
+        tg.run(Ad, Bd, bd, Cd, w.epilogue, stream=stream)
+
+    launch_ms, t_wall, clk = timed_steps(step, flush, args, dev, stream, world, local)
+    mean_ms, launch_stats = launch_summary(launch_ms, t_wall, args.steps)
     mean_ms_max = max_over_ranks(mean_ms, world)
     value = world * flops / (mean_ms_max * 1e-3) / 1e12
 
@@ -386,7 +532,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tgemm", "reference"], default="tgemm")
-    ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS) + sorted(si.ATTN_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -395,10 +541,11 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)          # at least 3 untimed warm-up steps
     world, rank, local = dist_setup()
+    attn = args.config in si.ATTN_WORKLOADS
     if args.impl == "reference":
-        rc = run_reference(args, world, rank)
+        rc = run_attention_reference(args, world, rank) if attn else run_reference(args, world, rank)
     else:
-        rc = run_tgemm_bench(args, world, rank, local)
+        rc = run_attention_bench(args, world, rank, local) if attn else run_tgemm_bench(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -46,7 +46,26 @@ struct AttnParams {
     float scale_log2;                 // log2(e) / sqrt(dim)
     void *O;
     unsigned int *status;
+#ifdef TGEMM_TRACE
+    unsigned long long *trace;        // trace builds: per-block cycle stamps of the first CTA
+#endif
 };
+
+// Trace builds only: clock64 stamps of the first CTA (blockIdx 0,0,0):
+// p.trace[kind * 32 + j] for key block j < 32; kind 0 softmax past the score
+// wait, 1 scores read, 2 exponentials done, 3 past the P.V wait, 4 P published
+// (softmax warp 4 lane 0); 5 MMA lane past the P wait, 6 P.V issued.
+#ifdef TGEMM_TRACE
+#define ATTN_STAMP(kind, j)                                                                   \
+    do {                                                                                      \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (j) < 32)                \
+            p.trace[(kind) * 32 + (j)] = clock64();                                           \
+    } while (0)
+#else
+#define ATTN_STAMP(kind, j) \
+    do {                    \
+    } while (0)
+#endif
 
 struct AttnSmem {
     static constexpr uint32_t kTile = kAttnBN * kAttnD * 2;          // 16 KiB: a [128 x 64] 16-bit tile
@@ -64,6 +83,14 @@ struct AttnSmem {
     static_assert(kBytes <= 232448, "shared memory budget");
 };
 
+// 2^x by the special-function unit (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22, results below 2^-126 flushed to zero, 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 template <bool kBf16, bool kCausal>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -76,7 +103,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (threadIdx.x == 0) atomicExch(p.status, kStatusLaunch);
         return;
     }
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // Causal tiles near the end of the sequence have the most key blocks: they
+    // are launched first so that the short ones fill in behind them.
+    // The query tile is the slowest grid index (z) so that launch order covers
+    // all heads and batches of one tile before the next.
+    const int qt = kCausal ? static_cast<int>(gridDim.z - 1 - blockIdx.z) : static_cast<int>(blockIdx.z);
+    const int h = blockIdx.x, b = blockIdx.y;
     const int q0 = qt * kAttnBM;
     const int nkb = (p.S + kAttnBN - 1) / kAttnBN;
     const int nblk = kCausal ? min(nkb, qt + 1) : nkb;     // blocks of equal size: the diagonal is block qt
@@ -184,6 +216,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         ok = false;
                         break;
                     }
+                    ATTN_STAMP(5, jp);
                     tc_fence_after();
                     const uint64_t v_desc =
                         sw128_desc(sbase + L::kKV + sp * 2 * L::kTile + L::kTile, kBK * 128, 1024);
@@ -195,6 +228,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                       (jp > 0 || k > 0) ? 1u : 0u);
                     mma_commit<1>(kv_empty(sp));
                     mma_commit<1>(pv_done);
+                    ATTN_STAMP(6, jp);
                 }
             }
             // All MMAs issued by this thread complete before TMEM is released.
@@ -218,6 +252,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int j = 0; j < nblk; ++j) {
             const int x = j & 1;
             if (!wait_all(s_full(x), static_cast<uint32_t>(j >> 1) & 1u)) { ok = false; break; }
+            if (warp == 4 && lane == 0) ATTN_STAMP(0, j);
             tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
@@ -229,35 +264,51 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_empty(x));
+            if (warp == 4 && lane == 0) ATTN_STAMP(1, j);
             // Scaled scores (log2 domain), masked keys at -inf, the block maximum.
+            // Only the last block (keys past the sequence) and, when causal, the
+            // diagonal block have masked keys.  Maxima and sums run in eight
+            // independent chains, combined at the end.
             const int key0 = j * kAttnBN;
-            float mx = -INFINITY;
+            const bool masked = (key0 + kAttnBN > p.S) || (kCausal && key0 + kAttnBN - 1 > q0);
+            float mx8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const int key = key0 + 32 * c + i;
                     float t = __uint_as_float(sr[c][i]) * p.scale_log2;
-                    if (key >= p.S || (kCausal && key > query)) t = -INFINITY;
+                    if (masked) {
+                        const int key = key0 + 32 * c + i;
+                        if (key >= p.S || (kCausal && key > query)) t = -INFINITY;
+                    }
                     sr[c][i] = __float_as_uint(t);
-                    mx = fmaxf(mx, t);
+                    mx8[i & 7] = fmaxf(mx8[i & 7], t);
                 }
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_new = fmaxf(m, mx);
             const float m_sub = (m_new == -INFINITY) ? 0.0f : m_new;
-            const float alpha = exp2f(m - m_sub);          // 0 on the first block (m = -inf)
-            float rowsum = 0.0f;
+            const float alpha = ex2_approx(m - m_sub);     // 0 on the first block (m = -inf)
+            float sum8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sum8[e] = 0.0f;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float pv = exp2f(__uint_as_float(sr[c][i]) - m_sub);
-                    rowsum += pv;
+                    const float pv = ex2_approx(__uint_as_float(sr[c][i]) - m_sub);
+                    sum8[i & 7] += pv;
                     sr[c][i] = __float_as_uint(pv);
                 }
+            const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l = l * alpha + rowsum;
             m = m_new;
+            if (warp == 4 && lane == 0) ATTN_STAMP(2, j);
             // P's buffer and the O accumulator are free once the previous P.V is done.
             if (j >= 1 && !wait_all(pv_done, static_cast<uint32_t>(j - 1) & 1u)) { ok = false; break; }
+            if (warp == 4 && lane == 0) ATTN_STAMP(3, j);
             tc_fence_after();
             // P row, 16-bit, 128B-swizzled: keys 64*t + 8*ch .. +8 of this row go to
             // 16-byte chunk ch ^ (row % 8) of row `row` in sub-tile t.
@@ -275,7 +326,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                  "r"(w[2]), "r"(w[3])
                                  : "memory");
                 }
-            if (j >= 1) {
+            // Rows whose maximum did not move have alpha = 1 exactly; a warp whose 32
+            // rows all kept theirs skips the (bit-neutral) rescale.
+            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
                 // O row *= exp2(m_old - m_new), in TMEM.
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -293,6 +346,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
+            if (warp == 4 && lane == 0) ATTN_STAMP(4, j);
         }
         if (ok && wait_all(pv_done, static_cast<uint32_t>(nblk - 1) & 1u)) {
             tc_fence_after();

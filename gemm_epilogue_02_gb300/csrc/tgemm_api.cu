@@ -818,8 +818,8 @@ cudaError_t launch_attention(DeviceInfo *d, unsigned bit, const CUtensorMap &tq,
             d->attn_attr_set |= bit;
         }
     }
-    const dim3 grid(static_cast<unsigned>(cdiv(p.S, kAttnBM)), static_cast<unsigned>(p.H),
-                    static_cast<unsigned>(p.B));
+    const dim3 grid(static_cast<unsigned>(p.H), static_cast<unsigned>(p.B),
+                    static_cast<unsigned>(cdiv(p.S, kAttnBM)));
     kernel<<<grid, kAttnThreads, AttnSmem::kBytes, s>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
@@ -833,7 +833,7 @@ extern "C" tgemm_status tgemm_attention_fwd(const void *Q, const void *K, const 
     if (batch < 0 || seq < 0 || heads < 0 || dim != kAttnD || (causal != 0 && causal != 1) ||
         (dtype != TGEMM_F16 && dtype != TGEMM_BF16))
         return TGEMM_ERR_INVALID_ARG;
-    if (batch > 65535 || heads > 65535 || seq > (int64_t(1) << 30) || batch * seq * heads > (int64_t(1) << 31))
+    if (batch > 65535 || heads > 65535 || seq > int64_t(65535) * kAttnBM || batch * seq * heads > (int64_t(1) << 31))
         return TGEMM_ERR_INVALID_ARG;
     if (batch == 0 || seq == 0 || heads == 0) return TGEMM_OK;
     if (!Q || !K || !V || !O) return TGEMM_ERR_INVALID_ARG;
@@ -863,6 +863,9 @@ extern "C" tgemm_status tgemm_attention_fwd(const void *Q, const void *K, const 
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dim)));
     p.O = O;
     p.status = d->status;
+#ifdef TGEMM_TRACE
+    p.trace = g_trace_buffer;
+#endif
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (bf16) e = causal ? launch_attention<true, true>(d, 1u, tq, tk, tv, p, s)

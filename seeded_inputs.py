@@ -112,3 +112,37 @@ def make_workload(w: Workload):
 def bits(x: torch.Tensor):
     """uint16 numpy view of a CPU fp16/bf16 tensor (the oracle's input form)."""
     return x.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Attention forward pass over [batch, seq, heads, dim] tensors."""
+    name: str
+    B: int
+    S: int
+    H: int
+    D: int
+    dtype: str
+    causal: bool
+    seed: int
+
+    @property
+    def flops(self) -> float:
+        # 4 * B * H * S^2 * D (two GEMMs), half of it when causal, as the page counts.
+        return 4.0 * self.B * self.H * self.S * self.S * self.D * (0.5 if self.causal else 1.0)
+
+
+# The FlashAttention workload of "TileLang で GPU カーネル設計を解説" §6:
+# (B, H, S, D) = (4, 8, 1024, 64), fp16, Q, K, V ~ N(0, 1); full and causal.
+ATTN_WORKLOADS = {
+    "fa": AttnWorkload("attention_fwd_4x1024x8x64_fp16", 4, 1024, 8, 64, "fp16", False, 22),
+    "fa_causal": AttnWorkload("attention_fwd_causal_4x1024x8x64_fp16", 4, 1024, 8, 64, "fp16", True, 23),
+}
+
+
+def make_attention_inputs(w: AttnWorkload):
+    """CPU tensors Q, K, V [B, S, H, D] in w.dtype: fp32 N(0, 1) draws in the
+    order Q, K, V from one seeded generator, rounded to the 16-bit format."""
+    g = torch.Generator("cpu").manual_seed(int(w.seed))
+    return [torch.randn(w.B, w.S, w.H, w.D, generator=g, dtype=torch.float32).to(DTYPES[w.dtype])
+            for _ in range(3)]
