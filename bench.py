@@ -46,7 +46,7 @@ def metric_for(w):
 DEFAULT_WORKLOAD = "c1"
 FLUSH_BYTES = 256 << 20            # > 2x the 129 MB L2
 KERNEL_SOURCES = ["gemm_epilogue_02_gb300/csrc/gemm_kernel.cuh", "gemm_epilogue_02_gb300/csrc/ptx.cuh",
-                  "gemm_epilogue_02_gb300/csrc/tgemm_api.cu"]
+                  "gemm_epilogue_02_gb300/csrc/attn_kernel.cuh", "gemm_epilogue_02_gb300/csrc/tgemm_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 

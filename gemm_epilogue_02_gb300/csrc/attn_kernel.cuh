@@ -13,19 +13,22 @@
 // blocks of 128:
 //
 //   warp 0      TMA producer: the Q tile once, then K and V tiles [128 x 64]
-//               into a 3-stage ring (one full / empty barrier per stage).
-//   warp 1      allocates TMEM (two 128-column score accumulators, a 64-column
+//               into a 2-stage ring (one full / empty barrier per stage).
+//   warp 1      allocates TMEM (a 128-column score accumulator, a 64-column
 //               output accumulator); one lane issues S_j = Q K_j^T (M = 128,
-//               N = 128, both operands K-major) into score buffer j % 2, then
-//               O += P_{j-1} V_{j-1} (P from shared memory, K-major; V
-//               MN-major, N = 64) once the softmax has published P_{j-1}.
-//   warps 4..7  softmax, one thread per query row (TMEM lane): read the row's
+//               N = 128, both operands K-major) as soon as the softmax has read
+//               S_{j-1}, then O += P_{j-1} V_{j-1} (P from shared memory,
+//               K-major; V MN-major, N = 64) once the softmax has published P_{j-1}.
+//   warps 2..5  softmax, one thread per query row (TMEM lane): read the row's
 //               128 scores, mask keys past the sequence (and after the query
 //               when causal), new running maximum, exp2 of the scaled scores,
 //               row sum; after the previous P.V has completed: write P (16-bit,
 //               128B-swizzled, two 64-key sub-tiles) and rescale the O row in
 //               TMEM by exp2(m_old - m_new); at the end divide by the row sum,
 //               round, store.
+//
+// Two CTAs share an SM (shared memory, TMEM and registers are sized for it),
+// so two independent softmax chains interleave on its schedulers.
 //
 // Every barrier wait is bounded as in the GEMM kernel; on expiry the CTA
 // records TGEMM_ERR_TIMEOUT, drains its copies and MMAs, frees TMEM and exits.
@@ -38,8 +41,9 @@ namespace tgemm {
 constexpr int kAttnBM = 128;          // query rows per CTA
 constexpr int kAttnBN = 128;          // keys per block
 constexpr int kAttnD = 64;            // head dimension
-constexpr int kAttnStages = 3;        // K/V ring depth
-constexpr int kAttnThreads = 256;     // warp 0 producer, warp 1 MMA, warps 4..7 softmax
+constexpr int kAttnStages = 2;        // K/V ring depth
+constexpr int kAttnThreads = 192;     // warp 0 producer, warp 1 MMA, warps 2..5 softmax
+constexpr int kAttnCtasPerSm = 2;     // two CTAs share an SM: their softmax chains interleave
 
 struct AttnParams {
     int B, S, H;
@@ -73,14 +77,15 @@ struct AttnSmem {
     static constexpr uint32_t kKV = kQ + kTile;                       // stage s: K, then V
     static constexpr uint32_t kP = kKV + kAttnStages * 2 * kTile;     // P: keys 0-63, then 64-127
     static constexpr uint32_t kBar = kP + 2 * kTile;
-    // q_full, kv_full[3], kv_empty[3], s_full[2], s_empty[2], p_full, pv_done, drain
-    static constexpr uint32_t kNumBars = 14;
+    // q_full, kv_full[2], kv_empty[2], s_full, s_empty, p_full, pv_done, drain
+    static constexpr uint32_t kNumBars = 10;
     static constexpr uint32_t kHolder = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kHolder + 4;
     static constexpr uint32_t kBytes = kAbort + 4;
-    static constexpr uint32_t kTmemCols = 512;                        // S0 at 0, S1 at 128, O at 256
+    static constexpr uint32_t kTmemCols = 256;                        // S at 0, O at 128 (two CTAs per SM)
     static_assert(kKV % 1024 == 0 && kP % 1024 == 0, "swizzled tiles need 1 KiB alignment");
-    static_assert(kBytes <= 232448, "shared memory budget");
+    // Per SM: 228 KiB of shared memory, of which each CTA also holds 1 KiB.
+    static_assert(kAttnCtasPerSm * (kBytes + 1024) <= 233472, "two CTAs per SM must fit in shared memory");
 };
 
 // 2^x by the special-function unit (PTX ex2.approx.ftz.f32: relative error
@@ -92,7 +97,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 template <bool kBf16, bool kCausal>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     using L = AttnSmem;
@@ -115,12 +120,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t bar0 = sbase + L::kBar;
     const uint32_t q_full = bar0;
     auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto kv_empty = [&](int s) { return bar0 + 8u * (4 + s); };
-    auto s_full = [&](int x) { return bar0 + 8u * (7 + x); };
-    auto s_empty = [&](int x) { return bar0 + 8u * (9 + x); };
-    const uint32_t p_full = bar0 + 8u * 11;
-    const uint32_t pv_done = bar0 + 8u * 12;
-    const uint32_t drain_bar = bar0 + 8u * 13;
+    auto kv_empty = [&](int s) { return bar0 + 8u * (1 + kAttnStages + s); };
+    const uint32_t s_full = bar0 + 8u * (1 + 2 * kAttnStages);
+    const uint32_t s_empty = bar0 + 8u * (2 + 2 * kAttnStages);
+    const uint32_t p_full = bar0 + 8u * (3 + 2 * kAttnStages);
+    const uint32_t pv_done = bar0 + 8u * (4 + 2 * kAttnStages);
+    const uint32_t drain_bar = bar0 + 8u * (5 + 2 * kAttnStages);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kHolder);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     const int warp = threadIdx.x >> 5;
@@ -132,10 +137,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
         }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(s_full(x), 1);
-            mbar_init(s_empty(x), 4);          // the four softmax warps
-        }
+        mbar_init(s_full, 1);
+        mbar_init(s_empty, 4);                 // the four softmax warps
         mbar_init(p_full, 4);
         mbar_init(pv_done, 1);
         mbar_init(drain_bar, 1);
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             prefetch_tmap(&tmV);
             mbar_arrive_expect_tx(q_full, L::kTile);
             tma_load_4d(sbase + L::kQ, &tmQ, q_full, 0, h, q0, b);
-            uint32_t uses[kAttnStages] = {0, 0, 0};
+            uint32_t uses[kAttnStages] = {};
             bool ok = true;
             for (int j = 0; j < nblk; ++j) {
                 const int s = j % kAttnStages;
@@ -192,22 +195,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             bool ok = wait_bar<false>(q_full, 0, abort_flag, p.status);
             for (int j = 0; ok && j <= nblk; ++j) {
                 if (j < nblk) {
+                    // The score buffer is free once the softmax has read S_{j-1}.
                     const int s = j % kAttnStages;
-                    const int x = j & 1;
                     if (!wait_bar<false>(kv_full(s), static_cast<uint32_t>(j / kAttnStages) & 1u, abort_flag,
                                          p.status) ||
-                        !wait_bar<true>(s_empty(x), (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag,
-                                        p.status)) {
+                        !wait_bar<true>(s_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint64_t k_desc = sw128_desc(sbase + L::kKV + s * 2 * L::kTile, 16, 1024);
-                    const uint32_t d_s = tmem_base + static_cast<uint32_t>(x * kAttnBN);
 #pragma unroll
                     for (int k = 0; k < kAttnD / kUmmaK; ++k)
-                        mma_f16_ss<1>(d_s, q_desc + k * 2, k_desc + k * 2, idesc_s, k > 0 ? 1u : 0u);
-                    mma_commit<1>(s_full(x));
+                        mma_f16_ss<1>(tmem_base, q_desc + k * 2, k_desc + k * 2, idesc_s, k > 0 ? 1u : 0u);
+                    mma_commit<1>(s_full);
                 }
                 if (j >= 1) {
                     const int jp = j - 1;
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         sw128_desc(sbase + L::kKV + sp * 2 * L::kTile + L::kTile, kBK * 128, 1024);
 #pragma unroll
                     for (int k = 0; k < kAttnBN / kUmmaK; ++k)
-                        mma_f16_ss<1>(tmem_base + 2 * kAttnBN,
+                        mma_f16_ss<1>(tmem_base + kAttnBN,
                                       p_desc + static_cast<uint32_t>(k >> 2) * (L::kTile >> 4) + (k & 3) * 2,
                                       v_desc + static_cast<uint32_t>(k) * (2048 >> 4), idesc_o,
                                       (jp > 0 || k > 0) ? 1u : 0u);
@@ -235,8 +236,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mma_commit_local<1>(drain_bar);
             drain_wait(drain_bar, 0);
         }
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ softmax
+    } else {
+        // ------------------------------------------------------------ softmax (warps 2..5)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const int query = q0 + row;
@@ -250,21 +251,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             return __shfl_sync(0xffffffffu, w, 0) != 0;
         };
         for (int j = 0; j < nblk; ++j) {
-            const int x = j & 1;
-            if (!wait_all(s_full(x), static_cast<uint32_t>(j >> 1) & 1u)) { ok = false; break; }
-            if (warp == 4 && lane == 0) ATTN_STAMP(0, j);
+            if (!wait_all(s_full, static_cast<uint32_t>(j) & 1u)) { ok = false; break; }
+            if (warp == 2 && lane == 0) ATTN_STAMP(0, j);
             tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(x * kAttnBN + 32 * c), sr[c]);
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(32 * c), sr[c]);
             tmem_wait_ld(sr[0]);
             tmem_wait_ld(sr[1]);
             tmem_wait_ld(sr[2]);
             tmem_wait_ld(sr[3]);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_empty(x));
-            if (warp == 4 && lane == 0) ATTN_STAMP(1, j);
+            if (lane == 0) mbar_arrive(s_empty);
+            if (warp == 2 && lane == 0) ATTN_STAMP(1, j);
             // Scaled scores (log2 domain), masked keys at -inf, the block maximum.
             // Only the last block (keys past the sequence) and, when causal, the
             // diagonal block have masked keys.  Maxima and sums run in eight
@@ -305,10 +305,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l = l * alpha + rowsum;
             m = m_new;
-            if (warp == 4 && lane == 0) ATTN_STAMP(2, j);
+            if (warp == 2 && lane == 0) ATTN_STAMP(2, j);
             // P's buffer and the O accumulator are free once the previous P.V is done.
             if (j >= 1 && !wait_all(pv_done, static_cast<uint32_t>(j - 1) & 1u)) { ok = false; break; }
-            if (warp == 4 && lane == 0) ATTN_STAMP(3, j);
+            if (warp == 2 && lane == 0) ATTN_STAMP(3, j);
             tc_fence_after();
             // P row, 16-bit, 128B-swizzled: keys 64*t + 8*ch .. +8 of this row go to
             // 16-byte chunk ch ^ (row % 8) of row `row` in sub-tile t.
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t o[32];
-                    const uint32_t ta = lane_base + static_cast<uint32_t>(2 * kAttnBN + 32 * c);
+                    const uint32_t ta = lane_base + static_cast<uint32_t>(kAttnBN + 32 * c);
                     tmem_ld_32x32b_x32(ta, o);
                     tmem_wait_ld(o);
 #pragma unroll
@@ -346,13 +346,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
-            if (warp == 4 && lane == 0) ATTN_STAMP(4, j);
+            if (warp == 2 && lane == 0) ATTN_STAMP(4, j);
         }
         if (ok && wait_all(pv_done, static_cast<uint32_t>(nblk - 1) & 1u)) {
             tc_fence_after();
             uint32_t o[2][32];
-            tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(2 * kAttnBN), o[0]);
-            tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(2 * kAttnBN + 32), o[1]);
+            tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kAttnBN), o[0]);
+            tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kAttnBN + 32), o[1]);
             tmem_wait_ld(o[0]);
             tmem_wait_ld(o[1]);
             if (query < p.S) {
