@@ -367,10 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto leader_tempty = [&](int a) { return (CG == 2) ? mapa_shared(tempty_bar(a), 0) : tempty_bar(a); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSLOT; ++s) {
-            mbar_init(full_bar(s), 1);             // rank 0's expect-tx arrival (bytes of the whole group)
-            mbar_init(empty_bar(s), 1);
-        }
+        for (int s = 0; s < NSLOT; ++s) mbar_init(full_bar(s), 1);   // rank 0's expect-tx arrival (bytes of the whole group)
+        for (int s = 0; s < STAGES; ++s) mbar_init(empty_bar(s), 1);  // one per stage: freed k-block by k-block
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), kEpiWarps * CG);
@@ -419,15 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // A unit starts on a slot boundary; its last slot may hold fewer k-blocks.
                 for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
                     const int nkb = min(KSUB, w.kb1 - kb);
-                    if (st_trace) TGEMM_STAGE_STAMP(0, kb - w.kb0);
-                    if (!wait_bar<true>(empty_bar(slot), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                    if (st_trace) TGEMM_STAGE_STAMP(1, kb - w.kb0);
-                    // Rank 0 announces the bytes of the whole group; with a CTA pair the
-                    // peer's copies report to rank 0's barrier (its transaction count may
-                    // dip below zero until the announcement lands, which is allowed).
                     const uint32_t fb = (CG == 1) ? full_bar(slot) : leader_full(slot);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), CG * tx * static_cast<uint32_t>(nkb));
-                    if (st_trace) TGEMM_STAGE_STAMP(6, kb - w.kb0);
                     auto load = [&](uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y) {
                         if constexpr (CG == 1) tma_load_2d(dst, m, fb, x, y);
                         else tma_load_2d_pair(dst, m, fb, x, y);
@@ -436,6 +426,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < KSUB; ++i) {
                         if (i >= nkb) break;
                         const int stage = slot * KSUB + i;
+                        // Each stage is refilled as soon as its own k-block's MMAs are done,
+                        // so a slot's first copies start one k-block earlier than a
+                        // whole-slot release would allow.
+                        if (st_trace && i == 0) TGEMM_STAGE_STAMP(0, kb - w.kb0);
+                        if (!wait_bar<true>(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                        if (i == 0) {
+                            if (st_trace) TGEMM_STAGE_STAMP(1, kb - w.kb0);
+                            // Rank 0 announces the bytes of the whole group and slot; with a
+                            // CTA pair the peer's copies report to rank 0's barrier (its
+                            // transaction count may dip below zero until the announcement
+                            // lands, which is allowed).
+                            if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), CG * tx * static_cast<uint32_t>(nkb));
+                            if (st_trace) TGEMM_STAGE_STAMP(6, kb - w.kb0);
+                        }
                         const int k0 = (kb + i) * kBK;
                         const uint32_t a_dst = sbase + L::kOffA + stage * L::kABytes;
                         const uint32_t b_dst = sbase + L::kOffB + stage * L::kBBytes;
@@ -467,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             load(b_dst, &tmB, k0, b_col);
                         }
                     }
+                    if (!ok) break;
                     if (st_trace) TGEMM_STAGE_STAMP(2, kb - w.kb0);
                     ++uses[slot];
                     if (++slot == NSLOT) { slot = 0; phase ^= 1u; }
@@ -528,17 +533,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 1; k < kBK / kUmmaK; ++k)
                         mma_f16_ss<CG>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
+                    mma_commit<CG>(empty_bar(first));      // frees the stage once read
 #pragma unroll
                     for (int i = 1; i < KSUB; ++i) {
-                        if (i >= nkb) break;
-                        const uint64_t adi = ad + static_cast<uint32_t>(i) * (L::kABytes >> 4);
-                        const uint64_t bdi = bd + static_cast<uint32_t>(i) * (L::kBBytes >> 4);
+                        // A stage the unit's last slot leaves unused is released all the
+                        // same, which keeps every stage's barrier phase in step with the slot.
+                        if (i < nkb) {
+                            const uint64_t adi = ad + static_cast<uint32_t>(i) * (L::kABytes >> 4);
+                            const uint64_t bdi = bd + static_cast<uint32_t>(i) * (L::kBBytes >> 4);
 #pragma unroll
-                        for (int k = 0; k < kBK / kUmmaK; ++k)
-                            mma_f16_ss<CG>(d_tmem, adi + k * a_kstep, bdi + k * b_kstep, idesc, 1u);
+                            for (int k = 0; k < kBK / kUmmaK; ++k)
+                                mma_f16_ss<CG>(d_tmem, adi + k * a_kstep, bdi + k * b_kstep, idesc, 1u);
+                        }
+                        mma_commit<CG>(empty_bar(first + i));
                     }
                     accumulate = 1u;
-                    mma_commit<CG>(empty_bar(slot));       // frees the ring slot once read
                     if (tile_i == 1) TGEMM_STAGE_STAMP(5, kb - kb0);
                     if (++slot == NSLOT) { slot = 0; phase ^= 1u; }
                 }
