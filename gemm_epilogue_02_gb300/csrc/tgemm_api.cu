@@ -466,9 +466,14 @@ bool encode_maps(const Cfg &cfg, const void *a, int64_t lda, int ta, const void 
 //    reduced by the last range to finish; each range keeps at least 4
 //    k-blocks; at most 16 ranges).
 //  * Otherwise the tiles of the last, partial wave (the remainder after whole
-//    waves) are cut into column parts (narrow tail) so that the wave's work
-//    spreads over more SMs; they run last, which also shortens the last
-//    epilogue.
+//    waves) are cut so that the wave's work spreads over more SMs: their k
+//    loops into 2-4 ranges when that many pieces fit one wave and each keeps
+//    at least 16 k-blocks (the pieces run first, and their last-arriver
+//    reductions overlap later tiles), else into column parts (narrow tail,
+//    run last).  The column parts load all of A for part of B and run at
+//    about 80 % of a whole tile's time for half its work; a k range costs
+//    its share of the k loop plus one partial write and read, which with
+//    8-k-block ranges (K = 1024) made the kernel 25 % slower than column parts.
 struct Plan {
     int split_k;
     int64_t split_first;    // tiles from here on are split in k
@@ -476,16 +481,26 @@ struct Plan {
     int narrow_parts;
 };
 
-Plan choose_plan(const Cfg &cfg, int64_t M, int64_t N, int64_t K, int num_sms) {
+// allow_split = false (callers without scratch for the partial sums) leaves
+// only the column-part tail.
+Plan choose_plan(const Cfg &cfg, int64_t M, int64_t N, int64_t K, int num_sms, bool allow_split = true) {
     const int64_t groups = cfg.cg == 2 ? num_sms / 2 : num_sms;
     const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn);
     const int64_t kb = cdiv(K, kBK);
-    if (const char *f = std::getenv("TGEMM_SPLIT_K")) return {std::max(1, std::atoi(f)), 0, 0, 1};
-    if (kb >= 8 && tiles * 2 <= groups)
-        return {static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({groups / tiles, kb / 4, 16}))), 0, 0, 1};
+    if (allow_split) {
+        if (const char *f = std::getenv("TGEMM_SPLIT_K")) return {std::max(1, std::atoi(f)), 0, 0, 1};
+        if (kb >= 8 && tiles * 2 <= groups)
+            return {static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({groups / tiles, kb / 4, 16}))), 0, 0, 1};
+    }
+    // TGEMM_TAIL_SPLIT: 0 = whole tiles only, 1 = column parts only.
     const char *tail = std::getenv("TGEMM_TAIL_SPLIT");
+    const int tail_mode = tail ? std::atoi(tail) : 2;
     const int64_t rem = tiles % groups;
-    if ((tail && std::atoi(tail) == 0) || rem == 0 || tiles < groups) return {1, tiles, tiles, 1};
+    if (tail_mode == 0 || rem == 0 || tiles < groups) return {1, tiles, tiles, 1};
+    if (allow_split && tail_mode == 2) {
+        const int64_t ranges = std::min<int64_t>({groups / rem, kb / 16, 4});
+        if (ranges >= 2) return {static_cast<int>(ranges), tiles - rem, tiles - rem, 1};
+    }
     const int s = narrow_parts_for(cfg, rem, groups);
     if (s < 2) return {1, tiles, tiles, 1};
     return {1, tiles, tiles - rem, s};
@@ -723,11 +738,9 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
     // No split-K here (its partials would need scratch); the narrow tail needs none.
-    const Plan plan = choose_plan(cfg, M, N, K, d->num_sms);
-    if (plan.split_k == 1) {
-        p.narrow_first = static_cast<int>(plan.narrow_first);
-        p.narrow_parts = plan.narrow_parts;
-    }
+    const Plan plan = choose_plan(cfg, M, N, K, d->num_sms, false);
+    p.narrow_first = static_cast<int>(plan.narrow_first);
+    p.narrow_parts = plan.narrow_parts;
     const cudaError_t e = launch_config(d, cfg, tma, tmb, tmb2, tmc, p, stream, bf16);
     if (e != cudaSuccess) {
         cudaGetLastError();

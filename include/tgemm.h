@@ -97,7 +97,8 @@ typedef enum {
  * Environment overrides of the work plan, for testing and tuning only (results
  * change at most by the split-K note below): TGEMM_FORCE_CFG (tile shape:
  * 256, 192, 128, 64, 256x2, 224x2, 128x2), TGEMM_SPLIT_K (k ranges for every
- * tile), TGEMM_TAIL_SPLIT=0 (no narrow tail), TGEMM_GROUP_M (row-blocks per
+ * tile), TGEMM_TAIL_SPLIT (the last partial wave's tiles: 0 = kept whole,
+ * 1 = cut into column parts only), TGEMM_GROUP_M (row-blocks per
  * column sweep), TGEMM_NO_B3D (one copy per 64-column sub-tile of B).
  *
  * Problems with too few output tiles to fill the GPU (few rows, e.g. decode
@@ -105,8 +106,10 @@ typedef enum {
  * pool scratch and the last CTA to finish a tile region adds them in a fixed
  * order before the epilogue, so results are deterministic; they may differ
  * in the last bits from an unsplit run (different summation order).  Larger
- * problems whose tiles leave a last, partial wave cut those tiles into
- * narrower column parts instead; that changes no result bit.
+ * problems whose tiles leave a last, partial wave cut those tiles the same
+ * way (2-4 k ranges, each at least 16 k-blocks, when the pieces fit one wave;
+ * same determinism, and those tiles may differ in the last bits from an
+ * unsplit run), else into narrower column parts, which change no result bit.
  *
  * Asynchrony: returns once the work is enqueued; the caller synchronises.
  * Thread safety: safe to call from several host threads.

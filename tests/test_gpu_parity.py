@@ -202,6 +202,44 @@ def test_narrow_tail(cuda_lib, monkeypatch, cfg, M, N, K, parts):
     assert np.array_equal(got, whole), "narrow parts changed the result bits"
 
 
+# ------------------------------------------------------------------ k-split tail
+# (cfg, M, N, K, ranges expected on a 152-SM GB300): the last, partial wave's
+# tiles have their k loops cut into ranges that run first; the last range to
+# finish adds the fp32 partials in range order before the epilogue.
+TAIL_SPLIT_CASES = [
+    ("256x2", 2048, 2560, 4096, 4),    # 8 x 10 = 80 pair tiles: 4 left, 64 k-blocks in 4 ranges
+    ("224x2", 2048, 2240, 3072, 3),    # 80 tiles of 224 columns: 4 left, 48 k-blocks in 3 ranges
+    ("256x2", 2048, 2404, 2000, 2),    # ragged k-block and a last column block of 100 columns
+    ("256", 2560, 2048, 4096, 4),      # 160 single-CTA tiles: 8 left over
+    ("128", 2560, 1088, 2070, 2),      # 180 tiles: 28 left; 33 k-blocks as 17 + 16
+]
+
+
+@pytest.mark.parametrize("cfg,M,N,K,ranges", TAIL_SPLIT_CASES)
+def test_k_split_tail(cuda_lib, monkeypatch, cfg, M, N, K, ranges):
+    """k ranges of the last wave's tiles: exact on integers, within the bound
+    on normal inputs, the same bits on every run, and within the bound of the
+    whole-tile result (only the summation order of those tiles changes)."""
+    monkeypatch.setenv("TGEMM_FORCE_CFG", cfg)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = cuda_lib.tgemm_plan(M, N, K, sms)
+    if sms == 152:
+        assert plan["split_k"] == ranges and plan["split_first"] == plan["tiles"] - plan["tiles"] % plan["groups"], plan
+    # One row of every 128-row block (every column is checked): each tile is sampled.
+    rows = sorted(set(sample_rows(M, n=32, seed=72)) | set(range(5, M, 128)) | set(range(M - 8, M)))
+    inputs, got = run_tgemm(cuda_lib, M, N, K, "fp16", "bias_relu", seed=71, kind="int")
+    ref = oracle_ref(inputs, M, N, K, "fp16", "bias_relu", rows=rows)
+    assert_bit_exact(got[rows], ref, "fp16", f"{cfg} k tail int")
+    inputs, got = run_tgemm(cuda_lib, M, N, K, "bf16", "bias_gelu", seed=72, kind="gelu")
+    check_epilogue(got[rows], inputs, M, N, K, "bf16", "bias_gelu", f"{cfg} k tail gelu", rows=rows)
+    _, again = run_tgemm(cuda_lib, M, N, K, "bf16", "bias_gelu", seed=72, kind="gelu")
+    assert np.array_equal(got, again), "k-split tail is not deterministic"
+    monkeypatch.setenv("TGEMM_TAIL_SPLIT", "0")
+    assert cuda_lib.tgemm_plan(M, N, K, sms)["split_k"] == 1
+    _, whole = run_tgemm(cuda_lib, M, N, K, "bf16", "bias_gelu", seed=72, kind="gelu")
+    check_epilogue(whole[rows], inputs, M, N, K, "bf16", "bias_gelu", f"{cfg} whole tiles gelu", rows=rows)
+
+
 @pytest.mark.parametrize("cfg", ["256x2", "128x2", "256", "192", "128", "64"])
 @pytest.mark.parametrize("M,N,K,ldb", [(700, 1024, 300, None),     # N a multiple of 64: one 3-D box per k-block
                                        (700, 1000, 300, 1024),     # last chunk past N inside the pitch

@@ -3,8 +3,10 @@ through tgemm_plan: host logic only, so it runs without a GPU.
 
 The expected plans are worked out by hand from the rules the planner states:
 CTA pairs with 256 x 256 tiles whenever those tiles fill every SM pair once;
-a last partial wave cut into column parts that still fit one wave; split-K
-only for problems with under half a wave of tiles.
+the tiles of a last partial wave cut in k into 2-4 ranges of at least 16
+k-blocks when those pieces fit one wave, else into column parts that still
+fit one wave; split-K of every tile only for problems with under half a wave
+of tiles.
 """
 import itertools
 import os
@@ -22,19 +24,41 @@ def _no_overrides(monkeypatch):
         monkeypatch.delenv(v, raising=False)
 
 
-def test_square_4096_pairs_with_a_narrow_tail():
-    # 16 x 16 = 256 tiles on 76 pairs: 3 whole waves and 28 tiles cut in two.
+def test_square_4096_pairs_with_a_k_split_tail():
+    # 16 x 16 = 256 tiles on 76 pairs: 3 whole waves; the 28 tiles left have
+    # their 64 k-blocks cut into 2 ranges (56 pieces <= 76; 3 would not fit).
     p = tg.tgemm_plan(4096, 4096, 4096, SMS)
     assert (p["bn"], p["cg"], p["tiles"], p["groups"]) == (256, 2, 256, 76)
+    assert (p["split_k"], p["split_first"], p["narrow_first"], p["narrow_parts"]) == (2, 228, 228, 1)
+    assert p["units"] == 2 * 28 + 228
+
+
+def test_square_4096_narrow_tail_on_request(monkeypatch):
+    # TGEMM_TAIL_SPLIT=1: the 28 tiles are cut into two column parts instead.
+    monkeypatch.setenv("TGEMM_TAIL_SPLIT", "1")
+    p = tg.tgemm_plan(4096, 4096, 4096, SMS)
     assert (p["split_k"], p["narrow_first"], p["narrow_parts"]) == (1, 228, 2)
     assert p["units"] == 228 + 2 * 28
 
 
 def test_square_8192():
-    # 32 x 32 = 1024 tiles: 13 waves of 76 and 36 tiles cut in two (72 <= 76).
+    # 32 x 32 = 1024 tiles: 13 waves of 76 and 36 tiles in two k ranges (72 <= 76).
     p = tg.tgemm_plan(8192, 8192, 8192, SMS)
     assert (p["bn"], p["cg"], p["tiles"]) == (256, 2, 1024)
-    assert (p["narrow_first"], p["narrow_parts"], p["units"]) == (988, 2, 988 + 72)
+    assert (p["split_k"], p["split_first"], p["narrow_parts"], p["units"]) == (2, 988, 1, 72 + 988)
+
+
+def test_tail_ranges_capped_by_k_and_four(monkeypatch):
+    # 20 x 8 = 160 single-CTA tiles, 8 left over: 19 ranges would fit, at most
+    # 4 are used; each range keeps 16 k-blocks, so K = 2048 (32 k-blocks) gives
+    # 2, and K = 1024 gives one, so the 8 tiles are cut into column parts.
+    monkeypatch.setenv("TGEMM_FORCE_CFG", "256")
+    p = tg.tgemm_plan(2560, 2048, 4096, SMS)
+    assert (p["tiles"], p["split_k"], p["split_first"], p["units"]) == (160, 4, 152, 152 + 32)
+    p = tg.tgemm_plan(2560, 2048, 2048, SMS)
+    assert (p["split_k"], p["split_first"], p["units"]) == (2, 152, 152 + 16)
+    p = tg.tgemm_plan(2560, 2048, 1024, SMS)
+    assert (p["split_k"], p["narrow_first"], p["narrow_parts"]) == (1, 152, 4)
 
 
 def test_decode_shape_splits_k():
@@ -84,9 +108,13 @@ def test_plan_invariants(sms):
         assert 0 <= nf <= sf <= p["tiles"]
         split_units = (p["tiles"] - sf) * sk if sk > 1 else 0
         assert p["units"] == split_units + nf + (sf - nf) * parts
-        if sk > 1:
-            assert p["tiles"] * 2 <= gmax and sf == 0
+        if sk > 1 and sf == 0:            # few tiles: every tile's k loop is cut
+            assert p["tiles"] * 2 <= gmax
             assert -(-(-(-K // 64)) // sk) >= 1
+        elif sk > 1:                        # the last partial wave's tiles are cut in k
+            assert p["tiles"] >= gmax and sf == p["tiles"] - p["tiles"] % gmax and nf == sf
+            assert 2 <= sk <= 4 and (p["tiles"] - sf) * sk <= gmax
+            assert (-(-K // 64)) // sk >= 16 and parts == 1
         if parts > 1:
             assert parts in (2, 4) and sk == 1
             assert (bn // cg // parts) % 64 == 0
