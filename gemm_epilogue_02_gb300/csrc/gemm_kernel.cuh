@@ -321,17 +321,19 @@ __device__ __forceinline__ void epi_math32(const uint32_t (&r)[32], const uint4 
     }
 }
 
-// KSUB: k-blocks per ring slot.  A slot has one full and one empty barrier and
-// KSUB stage buffers; the MMA lane waits once per slot (each wait costs the
-// lane a shared-memory round trip during which it issues nothing).
+// KSUB: k-blocks per ring slot.  The ring's STAGES buffers are used in turn,
+// one per k-block, each with its own empty barrier (released by the MMA
+// commit after that k-block); a slot of up to KSUB consecutive k-blocks has
+// one full barrier, so the MMA lane waits once per slot (each wait costs the
+// lane a shared-memory round trip during which it issues nothing).  STAGES
+// need not be a multiple of KSUB: slots simply wrap around the ring.
 template <int BN, int STAGES, int CG, int KSUB>
 __global__ void __launch_bounds__(kThreads, 1)
     tgemm_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmB2,
                        const __grid_constant__ CUtensorMap tmC, const KParams p) {
     using L = Smem<BN, STAGES, CG>;
-    static_assert(KSUB >= 1 && STAGES % KSUB == 0, "whole slots");
-    constexpr int NSLOT = STAGES / KSUB;
+    static_assert(KSUB >= 1 && KSUB <= STAGES, "a slot fits the ring");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
@@ -367,8 +369,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto leader_tempty = [&](int a) { return (CG == 2) ? mapa_shared(tempty_bar(a), 0) : tempty_bar(a); };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSLOT; ++s) mbar_init(full_bar(s), 1);   // rank 0's expect-tx arrival (bytes of the whole group)
-        for (int s = 0; s < STAGES; ++s) mbar_init(empty_bar(s), 1);  // one per stage: freed k-block by k-block
+        // Full barriers: one per slot in flight (a slot may hold a single k-block,
+        // so as many as stages); rank 0's expect-tx arrival carries the bytes of
+        // the whole group.  Empty barriers: one per stage, freed k-block by k-block.
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), kEpiWarps * CG);
@@ -398,10 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int slot = 0;
-            uint32_t phase = 0;
-            uint32_t uses[NSLOT];
-            for (int s = 0; s < NSLOT; ++s) uses[s] = 0;
+            // Ring position: stage / phase advance per k-block, full barrier /
+            // phase per slot of up to KSUB k-blocks (both wrap at STAGES).
+            int stage = 0, fbar = 0;
+            uint32_t phase = 0, fphase = 0;
+            uint32_t uses[STAGES];
+            for (int s = 0; s < STAGES; ++s) uses[s] = 0;
             bool ok = true;
             for (int u = group_id; u < p.num_units && ok; u += num_groups) {
                 const Unit w = unit_info(u, p, BN);
@@ -417,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // A unit starts on a slot boundary; its last slot may hold fewer k-blocks.
                 for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
                     const int nkb = min(KSUB, w.kb1 - kb);
-                    const uint32_t fb = (CG == 1) ? full_bar(slot) : leader_full(slot);
+                    const uint32_t fb = (CG == 1) ? full_bar(fbar) : leader_full(fbar);
                     auto load = [&](uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y) {
                         if constexpr (CG == 1) tma_load_2d(dst, m, fb, x, y);
                         else tma_load_2d_pair(dst, m, fb, x, y);
@@ -425,7 +434,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < KSUB; ++i) {
                         if (i >= nkb) break;
-                        const int stage = slot * KSUB + i;
                         // Each stage is refilled as soon as its own k-block's MMAs are done,
                         // so a slot's first copies start one k-block earlier than a
                         // whole-slot release would allow.
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // CTA pair the peer's copies report to rank 0's barrier (its
                             // transaction count may dip below zero until the announcement
                             // lands, which is allowed).
-                            if (rank == 0) mbar_arrive_expect_tx(full_bar(slot), CG * tx * static_cast<uint32_t>(nkb));
+                            if (rank == 0) mbar_arrive_expect_tx(full_bar(fbar), CG * tx * static_cast<uint32_t>(nkb));
                             if (st_trace) TGEMM_STAGE_STAMP(6, kb - w.kb0);
                         }
                         const int k0 = (kb + i) * kBK;
@@ -470,17 +478,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // narrow unit's MMA reads only the first width / CG of them.
                             load(b_dst, &tmB, k0, b_col);
                         }
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     }
                     if (!ok) break;
                     if (st_trace) TGEMM_STAGE_STAMP(2, kb - w.kb0);
-                    ++uses[slot];
-                    if (++slot == NSLOT) { slot = 0; phase ^= 1u; }
+                    ++uses[fbar];
+                    if (++fbar == STAGES) { fbar = 0; fphase ^= 1u; }
                 }
             }
             if (!ok) {
                 // Let every copy this thread started land before the CTA exits.
                 if (CG == 1 || rank == 0) {
-                    for (int s = 0; s < NSLOT; ++s)
+                    for (int s = 0; s < STAGES; ++s)
                         if (uses[s]) drain_wait(full_bar(s), (uses[s] - 1u) & 1u);
                 } else {
                     // The peer's copies report to rank 0's barriers: give them time to land.
@@ -493,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
-            int slot = 0;
-            uint32_t phase = 0;
+            int stage = 0, fbar = 0;    // ring position, as in the producer
+            uint32_t fphase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
@@ -522,34 +531,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = kb0; kb < kb1; kb += KSUB) {
                     const int nkb = min(KSUB, kb1 - kb);
                     if (tile_i == 1) TGEMM_STAGE_STAMP(3, kb - kb0);
-                    if (!wait_bar<false>(full_bar(slot), phase, abort_flag, p.status)) { ok = false; break; }
+                    if (!wait_bar<false>(full_bar(fbar), fphase, abort_flag, p.status)) { ok = false; break; }
                     if (tile_i == 1) TGEMM_STAGE_STAMP(4, kb - kb0);
                     tc_fence_after();
                     if (kb == kb0 && tile_i < 8) TGEMM_STAMP(8 + 4 * tile_i);
-                    const uint32_t first = static_cast<uint32_t>(slot * KSUB);
-                    const uint64_t ad = a_desc0 + first * (L::kABytes >> 4);
-                    const uint64_t bd = b_desc0 + first * (L::kBBytes >> 4);
-                    mma_f16_ss<CG>(d_tmem, ad, bd, idesc, accumulate);
 #pragma unroll
-                    for (int k = 1; k < kBK / kUmmaK; ++k)
-                        mma_f16_ss<CG>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
-                    mma_commit<CG>(empty_bar(first));      // frees the stage once read
+                    for (int i = 0; i < KSUB; ++i) {
+                        if (i >= nkb) break;
+                        const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (L::kABytes >> 4);
+                        const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (L::kBBytes >> 4);
 #pragma unroll
-                    for (int i = 1; i < KSUB; ++i) {
-                        // A stage the unit's last slot leaves unused is released all the
-                        // same, which keeps every stage's barrier phase in step with the slot.
-                        if (i < nkb) {
-                            const uint64_t adi = ad + static_cast<uint32_t>(i) * (L::kABytes >> 4);
-                            const uint64_t bdi = bd + static_cast<uint32_t>(i) * (L::kBBytes >> 4);
-#pragma unroll
-                            for (int k = 0; k < kBK / kUmmaK; ++k)
-                                mma_f16_ss<CG>(d_tmem, adi + k * a_kstep, bdi + k * b_kstep, idesc, 1u);
-                        }
-                        mma_commit<CG>(empty_bar(first + i));
+                        for (int k = 0; k < kBK / kUmmaK; ++k)
+                            mma_f16_ss<CG>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc,
+                                           (i == 0 && k == 0) ? accumulate : 1u);
+                        mma_commit<CG>(empty_bar(stage));      // frees the stage once read
+                        if (++stage == STAGES) stage = 0;
                     }
                     accumulate = 1u;
                     if (tile_i == 1) TGEMM_STAGE_STAMP(5, kb - kb0);
-                    if (++slot == NSLOT) { slot = 0; phase ^= 1u; }
+                    if (++fbar == STAGES) { fbar = 0; fphase ^= 1u; }
                 }
                 if (!ok) break;
                 mma_commit<CG>(tfull_bar(acc));            // accumulator ready for the epilogue
