@@ -44,6 +44,7 @@ constexpr int kAttnD = 64;            // head dimension
 constexpr int kAttnStages = 2;        // K/V ring depth
 constexpr int kAttnThreads = 192;     // warp 0 producer, warp 1 MMA, warps 2..5 softmax
 constexpr int kAttnCtasPerSm = 2;     // two CTAs share an SM: their softmax chains interleave
+constexpr float kAttnRescaleLog2 = 8.0f;   // running maximum kept until exceeded by 8 (a factor 256)
 
 struct AttnParams {
     int B, S, H;
@@ -117,6 +118,16 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     const int q0 = qt * kAttnBM;
     const int nkb = (p.S + kAttnBN - 1) / kAttnBN;
     const int nblk = kCausal ? min(nkb, qt + 1) : nkb;     // blocks of equal size: the diagonal is block qt
+#ifdef TGEMM_TRACE
+    // Trace builds: per-CTA entry / exit (globaltimer) and SM id, CTAs < 1024.
+    const int cta_lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    if (threadIdx.x == 0 && cta_lin < 1024) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        p.trace[4096 + 2 * cta_lin] = globaltimer_ns();
+        p.trace[8192 + cta_lin] = smid;
+    }
+#endif
     const uint32_t bar0 = sbase + L::kBar;
     const uint32_t q_full = bar0;
     auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
@@ -265,42 +276,56 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             __syncwarp();
             if (lane == 0) mbar_arrive(s_empty);
             if (warp == 2 && lane == 0) ATTN_STAMP(1, j);
-            // Scaled scores (log2 domain), masked keys at -inf, the block maximum.
-            // Only the last block (keys past the sequence) and, when causal, the
-            // diagonal block have masked keys.  Maxima and sums run in eight
-            // independent chains, combined at the end.
+            // Masked keys at -inf, then the block maximum of the raw scores (the
+            // scale is positive, so it commutes with the maximum).  Only the last
+            // block (keys past the sequence) and, when causal, the diagonal block
+            // have masked keys.  Maxima and sums run in eight independent chains,
+            // combined at the end.
             const int key0 = j * kAttnBN;
             const bool masked = (key0 + kAttnBN > p.S) || (kCausal && key0 + kAttnBN - 1 > q0);
+            if (masked) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int key = key0 + 32 * c + i;
+                        if (key >= p.S || (kCausal && key > query)) sr[c][i] = __float_as_uint(-INFINITY);
+                    }
+            }
             float mx8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float t = __uint_as_float(sr[c][i]) * p.scale_log2;
-                    if (masked) {
-                        const int key = key0 + 32 * c + i;
-                        if (key >= p.S || (kCausal && key > query)) t = -INFINITY;
-                    }
-                    sr[c][i] = __float_as_uint(t);
-                    mx8[i & 7] = fmaxf(mx8[i & 7], t);
-                }
+                for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
             const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-            const float m_new = fmaxf(m, mx);
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
+            // The running maximum m moves only when the block's maximum exceeds it
+            // by more than kAttnRescaleLog2: below that, exp2(t - m) stays under
+            // 2^kAttnRescaleLog2 and the sum and O keep their scale (any common
+            // shift of the exponents cancels in O / l), so O is rescaled rarely.
+            const bool grow = mx > m + kAttnRescaleLog2;                     // always true on the first finite block
+            const float m_new = grow ? mx : m;
             const float m_sub = (m_new == -INFINITY) ? 0.0f : m_new;
-            const float alpha = ex2_approx(m - m_sub);     // 0 on the first block (m = -inf)
+            const float alpha = grow ? ex2_approx(m - m_sub) : 1.0f;       // 0 when m was -inf
+            // P = exp2(scale * s - m): summed unrounded, kept as 16-bit pairs (the
+            // raw scores' registers free up as the pairs are formed).
             float sum8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) sum8[e] = 0.0f;
+            uint32_t pk[4][16];
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float pv = ex2_approx(__uint_as_float(sr[c][i]) - m_sub);
-                    sum8[i & 7] += pv;
-                    sr[c][i] = __float_as_uint(pv);
+                for (int i = 0; i < 32; i += 2) {
+                    const float x0 = fmaf(__uint_as_float(sr[c][i]), p.scale_log2, -m_sub);
+                    const float x1 = fmaf(__uint_as_float(sr[c][i + 1]), p.scale_log2, -m_sub);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    sum8[i & 7] += p0;
+                    sum8[(i + 1) & 7] += p1;
+                    pk[c][i / 2] = pack2<kBf16>(p0, p1);
                 }
             const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l = l * alpha + rowsum;
@@ -319,16 +344,15 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     const int c = (64 * t + 8 * ch) / 32, i0 = (64 * t + 8 * ch) % 32;
                     uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = pack2<kBf16>(__uint_as_float(sr[c][i0 + 2 * e]), __uint_as_float(sr[c][i0 + 2 * e + 1]));
+                    for (int e = 0; e < 4; ++e) w[e] = pk[c][i0 / 2 + e];
                     const uint32_t addr = sbase + L::kP + t * L::kTile + row * 128 + ((ch ^ (row & 7)) << 4);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
                                  "r"(w[2]), "r"(w[3])
                                  : "memory");
                 }
-            // Rows whose maximum did not move have alpha = 1 exactly; a warp whose 32
-            // rows all kept theirs skips the (bit-neutral) rescale.
-            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+            // Rows whose maximum did not move have alpha = 1; a warp whose 32 rows
+            // all kept theirs skips the rescale.
+            if (j >= 1 && __any_sync(0xffffffffu, grow)) {
                 // O row *= exp2(m_old - m_new), in TMEM.
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -378,6 +402,9 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc<1>(tmem_base, L::kTmemCols);
+#ifdef TGEMM_TRACE
+    if (threadIdx.x == 0 && cta_lin < 1024) p.trace[4096 + 2 * cta_lin + 1] = globaltimer_ns();
+#endif
 }
 
 }  // namespace tgemm
