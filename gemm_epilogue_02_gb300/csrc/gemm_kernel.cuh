@@ -789,16 +789,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float acc_v[32];
 #pragma unroll
                             for (int j = 0; j < 32; ++j) acc_v[j] = 0.0f;
+                            // Single-CTA tiles (the few-tile decode shapes): two ranges'
+                            // loads in flight per step, added in range order.  (The pair
+                            // kernels keep one range per step: their registers are full.)
+                            constexpr int kStep = (CG == 1) ? 2 : 1;
 #pragma unroll 1
-                            for (int rg = 0; rg < p.split_k; ++rg) {
-                                const float *src = region(rg) + sub * 1024 + lane * 4;
+                            for (int rg = 0; rg < p.split_k; rg += kStep) {
+                                const bool two = kStep == 2 && rg + 1 < p.split_k;
+                                const float *src0 = region(rg) + sub * 1024 + lane * 4;
+                                const float *src1 = region(two ? rg + 1 : rg) + sub * 1024 + lane * 4;
+                                float4 v0[8], v1[8];
 #pragma unroll
                                 for (int g = 0; g < 8; ++g) {
-                                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + g * 128));
-                                    acc_v[4 * g] += v.x;
-                                    acc_v[4 * g + 1] += v.y;
-                                    acc_v[4 * g + 2] += v.z;
-                                    acc_v[4 * g + 3] += v.w;
+                                    v0[g] = __ldcg(reinterpret_cast<const float4 *>(src0 + g * 128));
+                                    if constexpr (kStep == 2)
+                                        v1[g] = two ? __ldcg(reinterpret_cast<const float4 *>(src1 + g * 128))
+                                                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                                }
+#pragma unroll
+                                for (int g = 0; g < 8; ++g) {
+                                    acc_v[4 * g] += v0[g].x;
+                                    acc_v[4 * g + 1] += v0[g].y;
+                                    acc_v[4 * g + 2] += v0[g].z;
+                                    acc_v[4 * g + 3] += v0[g].w;
+                                }
+                                if (kStep == 2 && two) {
+#pragma unroll
+                                    for (int g = 0; g < 8; ++g) {
+                                        acc_v[4 * g] += v1[g].x;
+                                        acc_v[4 * g + 1] += v1[g].y;
+                                        acc_v[4 * g + 2] += v1[g].z;
+                                        acc_v[4 * g + 3] += v1[g].w;
+                                    }
                                 }
                             }
                             uint32_t rs[32];
