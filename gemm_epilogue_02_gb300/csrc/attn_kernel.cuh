@@ -15,17 +15,17 @@
 //   warp 0      TMA producer: the Q tile once, then K and V tiles [128 x 64]
 //               into a 2-stage ring (one full / empty barrier per stage).
 //   warp 1      allocates TMEM (a 128-column score accumulator, a 64-column
-//               output accumulator); one lane issues S_j = Q K_j^T (M = 128,
-//               N = 128, both operands K-major) as soon as the softmax has read
-//               S_{j-1}, then O += P_{j-1} V_{j-1} (P from shared memory,
-//               K-major; V MN-major, N = 64) once the softmax has published P_{j-1}.
+//               output accumulator, 64 columns for P); one lane issues
+//               S_j = Q K_j^T (M = 128, N = 128, both operands K-major) as soon
+//               as the softmax has read S_{j-1}, then O += P_{j-1} V_{j-1} (P
+//               from TMEM; V MN-major, N = 64) once the softmax has published P_{j-1}.
 //   warps 2..5  softmax, one thread per query row (TMEM lane): read the row's
 //               128 scores, mask keys past the sequence (and after the query
 //               when causal), new running maximum, exp2 of the scaled scores,
-//               row sum; after the previous P.V has completed: write P (16-bit,
-//               128B-swizzled, two 64-key sub-tiles) and rescale the O row in
-//               TMEM by exp2(m_old - m_new); at the end divide by the row sum,
-//               round, store.
+//               row sum; after the previous P.V has completed: write P (16-bit
+//               pairs) to TMEM and rescale the O row in TMEM by
+//               exp2(m_old - m_new) when the maximum moved; at the end divide by
+//               the row sum, round, store.
 //
 // Two CTAs share an SM (shared memory, TMEM and registers are sized for it),
 // so two independent softmax chains interleave on its schedulers.
@@ -76,15 +76,17 @@ struct AttnSmem {
     static constexpr uint32_t kTile = kAttnBN * kAttnD * 2;          // 16 KiB: a [128 x 64] 16-bit tile
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kKV = kQ + kTile;                       // stage s: K, then V
-    static constexpr uint32_t kP = kKV + kAttnStages * 2 * kTile;     // P: keys 0-63, then 64-127
-    static constexpr uint32_t kBar = kP + 2 * kTile;
+    static constexpr uint32_t kBar = kKV + kAttnStages * 2 * kTile;
     // q_full, kv_full[2], kv_empty[2], s_full, s_empty, p_full, pv_done, drain
     static constexpr uint32_t kNumBars = 10;
     static constexpr uint32_t kHolder = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kHolder + 4;
     static constexpr uint32_t kBytes = kAbort + 4;
-    static constexpr uint32_t kTmemCols = 256;                        // S at 0, O at 128 (two CTAs per SM)
-    static_assert(kKV % 1024 == 0 && kP % 1024 == 0, "swizzled tiles need 1 KiB alignment");
+    // TMEM columns: S at 0 (128, fp32), O at 128 (64, fp32), P at 192 (128 keys
+    // as 64 columns of 16-bit pairs, the second MMA's A operand); two CTAs per SM.
+    static constexpr uint32_t kTmemCols = 256;
+    static constexpr uint32_t kColO = 128, kColP = 192;
+    static_assert(kKV % 1024 == 0, "swizzled tiles need 1 KiB alignment");
     // Per SM: 228 KiB of shared memory, of which each CTA also holds 1 KiB.
     static_assert(kAttnCtasPerSm * (kBytes + 1024) <= 233472, "two CTAs per SM must fit in shared memory");
 };
@@ -200,9 +202,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             const uint32_t idesc_o = idesc_f16(kBf16, kAttnBM, kAttnD, false, true);
             // K-major tiles: 8-row groups 1 KiB apart, +32 B per 16-wide k step.
             // V (MN-major, one 64-column sub-tile): +2 KiB per 16 keys.
-            // P: two 64-key K-major sub-tiles 16 KiB apart.
             const uint64_t q_desc = sw128_desc(sbase + L::kQ, 16, 1024);
-            const uint64_t p_desc = sw128_desc(sbase + L::kP, 16, 1024);
             bool ok = wait_bar<false>(q_full, 0, abort_flag, p.status);
             for (int j = 0; ok && j <= nblk; ++j) {
                 if (j < nblk) {
@@ -232,12 +232,12 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     tc_fence_after();
                     const uint64_t v_desc =
                         sw128_desc(sbase + L::kKV + sp * 2 * L::kTile + L::kTile, kBK * 128, 1024);
+                    // P (A operand) from TMEM: 8 columns of 16-bit pairs per 16 keys.
 #pragma unroll
                     for (int k = 0; k < kAttnBN / kUmmaK; ++k)
-                        mma_f16_ss<1>(tmem_base + kAttnBN,
-                                      p_desc + static_cast<uint32_t>(k >> 2) * (L::kTile >> 4) + (k & 3) * 2,
-                                      v_desc + static_cast<uint32_t>(k) * (2048 >> 4), idesc_o,
-                                      (jp > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_ts(tmem_base + L::kColO, tmem_base + L::kColP + static_cast<uint32_t>(k) * 8u,
+                                   v_desc + static_cast<uint32_t>(k) * (2048 >> 4), idesc_o,
+                                   (jp > 0 || k > 0) ? 1u : 0u);
                     mma_commit<1>(kv_empty(sp));
                     mma_commit<1>(pv_done);
                     ATTN_STAMP(6, jp);
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             float sum8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) sum8[e] = 0.0f;
-            uint32_t pk[4][16];
+            uint32_t pk[2][32];     // P as 16-bit pairs: column 32 * t + e holds keys 64 t + 2e, +1
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     const float p1 = ex2_approx(x1);
                     sum8[i & 7] += p0;
                     sum8[(i + 1) & 7] += p1;
-                    pk[c][i / 2] = pack2<kBf16>(p0, p1);
+                    pk[c >> 1][(c & 1) * 16 + i / 2] = pack2<kBf16>(p0, p1);
                 }
             const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
             l = l * alpha + rowsum;
@@ -335,21 +335,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             if (j >= 1 && !wait_all(pv_done, static_cast<uint32_t>(j - 1) & 1u)) { ok = false; break; }
             if (warp == 2 && lane == 0) ATTN_STAMP(3, j);
             tc_fence_after();
-            // P row, 16-bit, 128B-swizzled: keys 64*t + 8*ch .. +8 of this row go to
-            // 16-byte chunk ch ^ (row % 8) of row `row` in sub-tile t.
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const int c = (64 * t + 8 * ch) / 32, i0 = (64 * t + 8 * ch) % 32;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) w[e] = pk[c][i0 / 2 + e];
-                    const uint32_t addr = sbase + L::kP + t * L::kTile + row * 128 + ((ch ^ (row & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                                 "r"(w[2]), "r"(w[3])
-                                 : "memory");
-                }
+            // P row -> TMEM columns kColP .. +63 of this row's lane: keys 2e, 2e+1
+            // packed in column e (the second MMA's A operand, K-major).
+            tmem_st_32x32b_x32(lane_base + L::kColP, pk[0]);
+            tmem_st_32x32b_x32(lane_base + L::kColP + 32u, pk[1]);
             // Rows whose maximum did not move have alpha = 1; a warp whose 32 rows
             // all kept theirs skips the rescale.
             if (j >= 1 && __any_sync(0xffffffffu, grow)) {
@@ -357,16 +346,15 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t o[32];
-                    const uint32_t ta = lane_base + static_cast<uint32_t>(kAttnBN + 32 * c);
+                    const uint32_t ta = lane_base + L::kColO + static_cast<uint32_t>(32 * c);
                     tmem_ld_32x32b_x32(ta, o);
                     tmem_wait_ld(o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                     tmem_st_32x32b_x32(ta, o);
                 }
-                tmem_wait_st();
             }
-            fence_proxy_async_shared();            // P visible to the tensor core
+            tmem_wait_st();                        // P (and any rescaled O) written
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
@@ -375,8 +363,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         if (ok && wait_all(pv_done, static_cast<uint32_t>(nblk - 1) & 1u)) {
             tc_fence_after();
             uint32_t o[2][32];
-            tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kAttnBN), o[0]);
-            tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(kAttnBN + 32), o[1]);
+            tmem_ld_32x32b_x32(lane_base + L::kColO, o[0]);
+            tmem_ld_32x32b_x32(lane_base + L::kColO + 32u, o[1]);
             tmem_wait_ld(o[0]);
             tmem_wait_ld(o[1]);
             if (query < p.S) {
