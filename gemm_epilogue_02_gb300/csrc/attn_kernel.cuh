@@ -13,7 +13,7 @@
 // blocks of 128:
 //
 //   warp 0      TMA producer: the Q tile once, then K and V tiles [128 x 64]
-//               into a 2-stage ring (one full / empty barrier per stage).
+//               into a 3-stage ring (one full / empty barrier per stage).
 //   warp 1      allocates TMEM (a 128-column score accumulator, a 64-column
 //               output accumulator, 64 columns for P); one lane issues
 //               S_j = Q K_j^T (M = 128, N = 128, both operands K-major) as soon
@@ -41,7 +41,7 @@ namespace tgemm {
 constexpr int kAttnBM = 128;          // query rows per CTA
 constexpr int kAttnBN = 128;          // keys per block
 constexpr int kAttnD = 64;            // head dimension
-constexpr int kAttnStages = 2;        // K/V ring depth
+constexpr int kAttnStages = 3;        // K/V ring depth
 constexpr int kAttnThreads = 192;     // warp 0 producer, warp 1 MMA, warps 2..5 softmax
 constexpr int kAttnCtasPerSm = 2;     // two CTAs share an SM: their softmax chains interleave
 constexpr float kAttnRescaleLog2 = 8.0f;   // running maximum kept until exceeded by 8 (a factor 256)
