@@ -327,7 +327,11 @@ __device__ __forceinline__ void epi_math32(const uint32_t (&r)[32], const uint4 
 // one full barrier, so the MMA lane waits once per slot (each wait costs the
 // lane a shared-memory round trip during which it issues nothing).  STAGES
 // need not be a multiple of KSUB: slots simply wrap around the ring.
-template <int BN, int STAGES, int CG, int KSUB>
+// MODE >= 0: the epilogue arithmetic is compiled for that one format x
+// activation (epi_math32<MODE >= 3, MODE % 3>), which keeps the kernel's code
+// small (the epilogue warps otherwise carry all six bodies and stall on
+// instruction fetch); -1: chosen at run time.
+template <int BN, int STAGES, int CG, int KSUB, int MODE = -1>
 __global__ void __launch_bounds__(kThreads, 1)
     tgemm_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmB2,
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     // Swizzled TMA tiles need a 1 KiB-aligned base.  The same for every CTA, so
     // all threads (and both CTAs of a pair) leave together before any barrier.
-    if (sbase & 1023u) {
+    if ((sbase & 1023u) || (MODE >= 0 && (p.is_bf16 ? 3 : 0) + p.act != MODE)) {
         if (threadIdx.x == 0) atomicExch(p.status, kStatusLaunch);
         return;
     }
@@ -668,13 +672,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Bias of these 32 columns from the warp's strip (broadcast reads).
                 const uint4 *bsrc = reinterpret_cast<const uint4 *>(bias_s + ((sub / SUBS) * CW + 32 * H));
                 uint32_t *out = packed + 16 * H;
-                switch (math_mode) {
-                    case 0: epi_math32<false, 0>(r, bsrc, out); break;
-                    case 1: epi_math32<false, 1>(r, bsrc, out); break;
-                    case 2: epi_math32<false, 2>(r, bsrc, out); break;
-                    case 3: epi_math32<true, 0>(r, bsrc, out); break;
-                    case 4: epi_math32<true, 1>(r, bsrc, out); break;
-                    default: epi_math32<true, 2>(r, bsrc, out); break;
+                if constexpr (MODE >= 0) {
+                    epi_math32<(MODE >= 3), MODE % 3>(r, bsrc, out);
+                } else {
+                    switch (math_mode) {
+                        case 0: epi_math32<false, 0>(r, bsrc, out); break;
+                        case 1: epi_math32<false, 1>(r, bsrc, out); break;
+                        case 2: epi_math32<false, 2>(r, bsrc, out); break;
+                        case 3: epi_math32<true, 0>(r, bsrc, out); break;
+                        case 4: epi_math32<true, 1>(r, bsrc, out); break;
+                        default: epi_math32<true, 2>(r, bsrc, out); break;
+                    }
                 }
                 TGEMM_EPI_STAMP(24 + (sub & 3));
                 if constexpr (H != SUBS - 1) return;

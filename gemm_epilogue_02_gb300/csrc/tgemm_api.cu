@@ -305,11 +305,11 @@ Cfg choose_config(int64_t M, int64_t N, int64_t K, int num_sms) {
     return best;
 }
 
-template <int BN, int ST, int CG, int KSUB>
-cudaError_t launch_fused(DeviceInfo *d, int bit, const CUtensorMap &ta, const CUtensorMap &tb,
+template <int BN, int ST, int CG, int KSUB, int MODE = -1>
+cudaError_t launch_fused(DeviceInfo *d, unsigned bit, const CUtensorMap &ta, const CUtensorMap &tb,
                          const CUtensorMap &tb2, const CUtensorMap &tc, const KParams &p, int64_t tiles, cudaStream_t s) {
     using L = Smem<BN, ST, CG>;
-    auto kernel = tgemm_fused_kernel<BN, ST, CG, KSUB>;
+    auto kernel = tgemm_fused_kernel<BN, ST, CG, KSUB, MODE>;
     int max_groups = d->num_sms;
     {
         std::lock_guard<std::mutex> g(d->mu);
@@ -411,7 +411,16 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
         case 1: return launch_fused<256, 4, 1, 1>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
         case 2: return launch_fused<128, 6, 1, 1>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
         case 4: return launch_fused<64, 8, 1, 1>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
-        case 8: return launch_fused<256, 6, 2, 2>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
+        case 8:
+            // The main shape: one kernel per format x activation (smaller code).
+            switch ((bf16 ? 3 : 0) + p.act) {
+                case 0: return launch_fused<256, 6, 2, 2, 0>(d, 128u << 0, ta, tb, tb2, tc, p, units, s);
+                case 1: return launch_fused<256, 6, 2, 2, 1>(d, 128u << 1, ta, tb, tb2, tc, p, units, s);
+                case 2: return launch_fused<256, 6, 2, 2, 2>(d, 128u << 2, ta, tb, tb2, tc, p, units, s);
+                case 3: return launch_fused<256, 6, 2, 2, 3>(d, 128u << 3, ta, tb, tb2, tc, p, units, s);
+                case 4: return launch_fused<256, 6, 2, 2, 4>(d, 128u << 4, ta, tb, tb2, tc, p, units, s);
+                default: return launch_fused<256, 6, 2, 2, 5>(d, 128u << 5, ta, tb, tb2, tc, p, units, s);
+            }
         case 16: return launch_fused<128, 8, 2, 2>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
         case 32: return launch_fused<192, 4, 1, 1>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
         default: return launch_fused<224, 6, 2, 2>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
