@@ -98,6 +98,10 @@ struct KParams {
     int b_3d;                  // B [K, N] through a 3-D map (tmB): all BN/CG columns of a k-block in
                                // one box; narrow units then use the 2-D map tmB2
     uint32_t stage_tx;         // bytes one CTA loads per ring stage (depends on the layouts)
+    // Testing only (0 otherwise): extra bytes announced for the first ring slot,
+    // which then never completes, so that the operand wait runs out and the
+    // timeout path (status word, drain, TMEM release) is exercised.
+    uint32_t test_extra_tx;
     uint32_t idesc;
     unsigned int *status;      // device status word
 #ifdef TGEMM_TRACE
@@ -449,7 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // CTA pair the peer's copies report to rank 0's barrier (its
                             // transaction count may dip below zero until the announcement
                             // lands, which is allowed).
-                            if (rank == 0) mbar_arrive_expect_tx(full_bar(fbar), CG * tx * static_cast<uint32_t>(nkb));
+                            if (rank == 0)
+                                mbar_arrive_expect_tx(full_bar(fbar), CG * tx * static_cast<uint32_t>(nkb) +
+                                                                          (uses[fbar] == 0 && fbar == 0 ? p.test_extra_tx : 0u));
+                            ++uses[fbar];   // counted once its first copy may be in flight (drain below)
                             if (st_trace) TGEMM_STAGE_STAMP(6, kb - w.kb0);
                         }
                         const int k0 = (kb + i) * kBK;
@@ -486,7 +493,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!ok) break;
                     if (st_trace) TGEMM_STAGE_STAMP(2, kb - w.kb0);
-                    ++uses[fbar];
                     if (++fbar == STAGES) { fbar = 0; fphase ^= 1u; }
                 }
             }

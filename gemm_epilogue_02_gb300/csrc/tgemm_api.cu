@@ -605,6 +605,8 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     p.split_first = static_cast<int>(plan.split_first);
     p.narrow_first = static_cast<int>(plan.narrow_first);
     p.narrow_parts = plan.narrow_parts;
+    if (const char *e = std::getenv("TGEMM_TEST_STALL"))
+        if (std::atoi(e) != 0) p.test_extra_tx = 16;   // testing only: see KParams::test_extra_tx
     if (p.split_k > 1) {
         const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn) - plan.split_first;
         const int64_t pbytes = tiles * p.split_k * partial_floats_per_unit(cfg) * 4;
