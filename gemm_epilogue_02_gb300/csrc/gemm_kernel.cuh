@@ -511,7 +511,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && rank == 0) {
+        // The whole warp runs the loop (warp-uniform control flow, so the
+        // descriptors stay warp-uniform values); one elected lane issues every
+        // MMA and commit, since a commit tracks the MMAs of the thread that
+        // issues it.  Issuing from a lone divergent lane took about twice as
+        // many cycles per MMA.
+        if (rank == 0) {
+            const bool issuer = elect_one_sync() != 0u;
             int stage = 0, fbar = 0;    // ring position, as in the producer
             uint32_t fphase = 0;
             int acc = 0;
@@ -545,29 +551,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (tile_i == 1) TGEMM_STAGE_STAMP(4, kb - kb0);
                     tc_fence_after();
                     if (kb == kb0 && tile_i < 8) TGEMM_STAMP(8 + 4 * tile_i);
+                    if (issuer) {
 #pragma unroll
-                    for (int i = 0; i < KSUB; ++i) {
-                        if (i >= nkb) break;
-                        const uint64_t ad = a_desc0 + static_cast<uint32_t>(stage) * (L::kABytes >> 4);
-                        const uint64_t bd = b_desc0 + static_cast<uint32_t>(stage) * (L::kBBytes >> 4);
+                        for (int i = 0; i < KSUB; ++i) {
+                            if (i >= nkb) break;
+                            const int st = (stage + i < STAGES) ? stage + i : stage + i - STAGES;   // slots wrap
+                            const uint64_t ad = a_desc0 + static_cast<uint32_t>(st) * (L::kABytes >> 4);
+                            const uint64_t bd = b_desc0 + static_cast<uint32_t>(st) * (L::kBBytes >> 4);
 #pragma unroll
-                        for (int k = 0; k < kBK / kUmmaK; ++k)
-                            mma_f16_ss<CG>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc,
-                                           (i == 0 && k == 0) ? accumulate : 1u);
-                        mma_commit<CG>(empty_bar(stage));      // frees the stage once read
-                        if (++stage == STAGES) stage = 0;
+                            for (int k = 0; k < kBK / kUmmaK; ++k)
+                                mma_f16_ss<CG>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc,
+                                               (i == 0 && k == 0) ? accumulate : 1u);
+                            mma_commit<CG>(empty_bar(st));      // frees the stage once read
+                        }
                     }
+                    stage += nkb;
+                    if (stage >= STAGES) stage -= STAGES;
                     accumulate = 1u;
                     if (tile_i == 1) TGEMM_STAGE_STAMP(5, kb - kb0);
                     if (++fbar == STAGES) { fbar = 0; fphase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit<CG>(tfull_bar(acc));            // accumulator ready for the epilogue
+                if (issuer) mma_commit<CG>(tfull_bar(acc));   // accumulator ready for the epilogue
                 if (tile_i < 8) TGEMM_STAMP(9 + 4 * tile_i);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
-            // All MMAs issued by this thread complete before TMEM is released.
-            mma_commit_local<CG>(drain_bar);
+            // All MMAs issued by the elected lane complete before TMEM is released.
+            if (issuer) mma_commit_local<CG>(drain_bar);
             drain_wait(drain_bar, 0);
         }
     } else {
