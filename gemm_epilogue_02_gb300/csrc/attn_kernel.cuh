@@ -15,7 +15,7 @@
 //   warp 0      TMA producer: the Q tile once, then K and V tiles [128 x 64]
 //               into a 3-stage ring (one full / empty barrier per stage).
 //   warp 1      allocates TMEM (a 128-column score accumulator, a 64-column
-//               output accumulator, 64 columns for P); one lane issues
+//               output accumulator, 64 columns for P); an elected lane issues
 //               S_j = Q K_j^T (M = 128, N = 128, both operands K-major) as soon
 //               as the softmax has read S_{j-1}, then O += P_{j-1} V_{j-1} (P
 //               from TMEM; V MN-major, N = 64) once the softmax has published P_{j-1}.
@@ -197,7 +197,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        {
+            // Warp-uniform loop; one elected lane issues the MMAs and commits
+            // (a commit tracks the MMAs of the thread that issues it).
+            const bool issuer = elect_one_sync() != 0u;
             const uint32_t idesc_s = idesc_f16(kBf16, kAttnBM, kAttnBN, false, false);
             const uint32_t idesc_o = idesc_f16(kBf16, kAttnBM, kAttnD, false, true);
             // K-major tiles: 8-row groups 1 KiB apart, +32 B per 16-wide k step.
@@ -216,10 +219,12 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     }
                     tc_fence_after();
                     const uint64_t k_desc = sw128_desc(sbase + L::kKV + s * 2 * L::kTile, 16, 1024);
+                    if (issuer) {
 #pragma unroll
-                    for (int k = 0; k < kAttnD / kUmmaK; ++k)
-                        mma_f16_ss<1>(tmem_base, q_desc + k * 2, k_desc + k * 2, idesc_s, k > 0 ? 1u : 0u);
-                    mma_commit<1>(s_full);
+                        for (int k = 0; k < kAttnD / kUmmaK; ++k)
+                            mma_f16_ss<1>(tmem_base, q_desc + k * 2, k_desc + k * 2, idesc_s, k > 0 ? 1u : 0u);
+                        mma_commit<1>(s_full);
+                    }
                 }
                 if (j >= 1) {
                     const int jp = j - 1;
@@ -233,18 +238,20 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     const uint64_t v_desc =
                         sw128_desc(sbase + L::kKV + sp * 2 * L::kTile + L::kTile, kBK * 128, 1024);
                     // P (A operand) from TMEM: 8 columns of 16-bit pairs per 16 keys.
+                    if (issuer) {
 #pragma unroll
-                    for (int k = 0; k < kAttnBN / kUmmaK; ++k)
-                        mma_f16_ts(tmem_base + L::kColO, tmem_base + L::kColP + static_cast<uint32_t>(k) * 8u,
-                                   v_desc + static_cast<uint32_t>(k) * (2048 >> 4), idesc_o,
-                                   (jp > 0 || k > 0) ? 1u : 0u);
-                    mma_commit<1>(kv_empty(sp));
-                    mma_commit<1>(pv_done);
+                        for (int k = 0; k < kAttnBN / kUmmaK; ++k)
+                            mma_f16_ts(tmem_base + L::kColO, tmem_base + L::kColP + static_cast<uint32_t>(k) * 8u,
+                                       v_desc + static_cast<uint32_t>(k) * (2048 >> 4), idesc_o,
+                                       (jp > 0 || k > 0) ? 1u : 0u);
+                        mma_commit<1>(kv_empty(sp));
+                        mma_commit<1>(pv_done);
+                    }
                     ATTN_STAMP(6, jp);
                 }
             }
-            // All MMAs issued by this thread complete before TMEM is released.
-            mma_commit_local<1>(drain_bar);
+            // All MMAs issued by the elected lane complete before TMEM is released.
+            if (issuer) mma_commit_local<1>(drain_bar);
             drain_wait(drain_bar, 0);
         }
     } else {

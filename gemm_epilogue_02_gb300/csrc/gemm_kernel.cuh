@@ -273,11 +273,18 @@ __device__ __forceinline__ float epi_relu(float v) {
 }
 
 // The tanh-form GELU of "TileLang で GPU カーネル設計を解説" §4, written as a
-// sigmoid: x / (1 + exp(-1.5957691216 (x + 0.044715 x^3))).  Large negative x
-// gives exp -> inf and x * 0 = -0; NaN propagates.
+// sigmoid: x / (1 + exp(-1.5957691216 (x + 0.044715 x^3))).  The exponential
+// is taken base 2 with the constants folded, exp(-1.5957691216 (x + 0.044715
+// x^3)) = 2^(x (c1 + c2 x^2)), c1 = -1.5957691216 log2(e), c2 = 0.044715 c1,
+// so that each element costs three multiply-adds before the hardware 2^z
+// (`ex2.approx`) and the reciprocal; in fp32 the folded form stays within
+// about 2e-7 |x| of the exact function.  Large negative x gives 2^z -> inf
+// and x * 0 = -0; NaN propagates.
 __device__ __forceinline__ float epi_gelu(float x) {
-    const float u = 1.5957691216f * fmaf(0.044715f * x, x * x, x);
-    return __fdividef(x, 1.0f + __expf(-u));
+    const float z = x * fmaf(-0.10294324f, x * x, -2.3022082f);
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z));
+    return __fdividef(x, 1.0f + e);
 }
 
 template <bool kBf16>
