@@ -100,10 +100,13 @@ typedef enum {
  * tile), TGEMM_TAIL_SPLIT (the last partial wave's tiles: 0 = kept whole,
  * 1 = cut into column parts only), TGEMM_GROUP_M (row-blocks per
  * column sweep), TGEMM_NO_B3D (one copy per 64-column sub-tile of B).
- * TGEMM_TEST_STALL=1 (testing the failure path only) makes tgemm_run's kernel
- * announce 16 bytes that never arrive for its first operand slot: its
+ * TGEMM_TEST_STALL=1 (testing the failure path only) makes the GEMM kernel of
+ * each call announce 16 bytes that never arrive for its first operand slot: its
  * operand wait runs out after 2 s, the kernel records TGEMM_ERR_TIMEOUT in the
  * device status word, drains and returns (C is left incomplete).
+ * TGEMM_TRACE_MAX_GROUPS caps the persistent CTA groups in trace builds
+ * (compiled with -DTGEMM_TRACE, never the product build) and is ignored
+ * otherwise.
  *
  * Problems with too few output tiles to fill the GPU (few rows, e.g. decode
  * shapes) split the k loop of each tile across CTAs: fp32 partial sums go to

@@ -34,6 +34,18 @@ def test_library_exports_every_declared_symbol():
     assert tg.tgemm_version() == 0x000100
 
 
+def test_header_documents_every_environment_variable_the_library_reads():
+    src_dir = os.path.join(ROOT, "gemm_epilogue_02_gb300", "csrc")
+    names = set()
+    for f in os.listdir(src_dir):
+        if f.endswith((".cu", ".cuh")):
+            names |= set(re.findall(r'getenv\("(\w+)"\)', open(os.path.join(src_dir, f)).read()))
+    assert names, "no environment variables found"
+    header = open(HEADER).read()
+    missing = sorted(n for n in names if n not in header)
+    assert not missing, missing
+
+
 def test_status_strings():
     for code, name in tg.STATUS.items():
         assert tg.tgemm_status_string(code).startswith(name)
