@@ -77,8 +77,17 @@ struct AttnSmem {
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kKV = kQ + kTile;                       // stage s: K, then V
     static constexpr uint32_t kBar = kKV + kAttnStages * 2 * kTile;
-    // q_full, kv_full[2], kv_empty[2], s_full, s_empty, p_full, pv_done, drain
-    static constexpr uint32_t kNumBars = 10;
+    // Barrier slots (8 bytes each): q_full, kv_full[stages], kv_empty[stages],
+    // s_full, s_empty, p_full, pv_done, drain.
+    static constexpr uint32_t kBarQFull = 0;
+    static constexpr uint32_t kBarKVFull = 1;
+    static constexpr uint32_t kBarKVEmpty = kBarKVFull + kAttnStages;
+    static constexpr uint32_t kBarSFull = kBarKVEmpty + kAttnStages;
+    static constexpr uint32_t kBarSEmpty = kBarSFull + 1;
+    static constexpr uint32_t kBarPFull = kBarSEmpty + 1;
+    static constexpr uint32_t kBarPVDone = kBarPFull + 1;
+    static constexpr uint32_t kBarDrain = kBarPVDone + 1;
+    static constexpr uint32_t kNumBars = kBarDrain + 1;
     static constexpr uint32_t kHolder = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kHolder + 4;
     static constexpr uint32_t kBytes = kAbort + 4;
@@ -131,14 +140,14 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     }
 #endif
     const uint32_t bar0 = sbase + L::kBar;
-    const uint32_t q_full = bar0;
-    auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-    auto kv_empty = [&](int s) { return bar0 + 8u * (1 + kAttnStages + s); };
-    const uint32_t s_full = bar0 + 8u * (1 + 2 * kAttnStages);
-    const uint32_t s_empty = bar0 + 8u * (2 + 2 * kAttnStages);
-    const uint32_t p_full = bar0 + 8u * (3 + 2 * kAttnStages);
-    const uint32_t pv_done = bar0 + 8u * (4 + 2 * kAttnStages);
-    const uint32_t drain_bar = bar0 + 8u * (5 + 2 * kAttnStages);
+    const uint32_t q_full = bar0 + 8u * L::kBarQFull;
+    auto kv_full = [&](int s) { return bar0 + 8u * (L::kBarKVFull + s); };
+    auto kv_empty = [&](int s) { return bar0 + 8u * (L::kBarKVEmpty + s); };
+    const uint32_t s_full = bar0 + 8u * L::kBarSFull;
+    const uint32_t s_empty = bar0 + 8u * L::kBarSEmpty;
+    const uint32_t p_full = bar0 + 8u * L::kBarPFull;
+    const uint32_t pv_done = bar0 + 8u * L::kBarPVDone;
+    const uint32_t drain_bar = bar0 + 8u * L::kBarDrain;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kHolder);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kAbort);
     const int warp = threadIdx.x >> 5;
