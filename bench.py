@@ -43,10 +43,11 @@ METRIC_GELU = "fused GEMM+bias+GELU TFLOP/s (2MNK/t) on 1 GB300; % of dense fp16
 
 def metric_for(w):
     return METRIC_GELU if "gelu" in w.epilogue else METRIC
-DEFAULT_WORKLOAD = "c1"
+DEFAULT_WORKLOAD = "c2"
 FLUSH_BYTES = 256 << 20            # > 2x the 129 MB L2
 KERNEL_SOURCES = ["gemm_epilogue_02_gb300/csrc/gemm_kernel.cuh", "gemm_epilogue_02_gb300/csrc/ptx.cuh",
-                  "gemm_epilogue_02_gb300/csrc/attn_kernel.cuh", "gemm_epilogue_02_gb300/csrc/tgemm_api.cu"]
+                  "gemm_epilogue_02_gb300/csrc/attn_kernel.cuh", "gemm_epilogue_02_gb300/csrc/aux_kernels.cuh",
+                  "gemm_epilogue_02_gb300/csrc/tgemm_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
@@ -59,13 +60,16 @@ def kernel_hash() -> str:
 
 
 def measured_peaks():
+    """Roofline denominators: the measured dense bf16 burst and sustained
+    TFLOP/s and HBM copy GB/s, else the fallback figures."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+        return {"tflops": float(d["bf16_tflops"]), "hbm": float(d["hbm_gbs"]), "kind": "measured",
+                "tflops_sustained": float(d["bf16_tflops_sustained"]) if "bf16_tflops_sustained" in d else None}
     except (OSError, KeyError, ValueError):
-        return 1900.0, 6800.0, "fallback"
+        return {"tflops": 1900.0, "hbm": 6800.0, "kind": "fallback", "tflops_sustained": 1700.0}
 
 
 def recorded_traffic(workload: str):
@@ -195,58 +199,81 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def cpu_oracle_sample(w, target_s: float):
-    """Time the fp64 oracle (as it stands) on a bounded sample of rows: the row
-    count grows until one run takes about target_s seconds (or covers all rows)."""
-    import oracle
-    A, B, bias = si.make_workload(w)
-    ba, bb = si.bits(A), si.bits(B)
-    bc = si.bits(bias) if bias is not None else None
-    epi = si.EPILOGUES[w.epilogue]
-    dt = oracle.dtype_code(w.dtype)
-    cores = oracle.max_threads()
-    rows_n = min(w.M, max(cores, 1))
-    while True:
+class OracleSample:
+    """The fp64 oracle (as it stands) on the first rows of a workload.  Each call
+    decodes all of B once (serially) before the rows run in parallel, so a call
+    costs a fixed part plus a part per row; `fixed_s` (a one-row call) is
+    reported beside every figure so the two CPU legs can be read together."""
+
+    def __init__(self, w):
+        import oracle
+        self.w = w
+        A, B, bias = si.make_workload(w)
+        self.args = (si.bits(A), si.bits(B), si.bits(bias) if bias is not None else None)
+        self.epi = si.EPILOGUES[w.epilogue]
+        self.dt = oracle.dtype_code(w.dtype)
+        self.cores = oracle.max_threads()
+        self.fixed_s = self.time(1)
+
+    def time(self, rows_n: int) -> float:
+        import oracle
+        w = self.w
         t0 = time.perf_counter()
-        oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=list(range(rows_n)))
-        t = time.perf_counter() - t0
-        if t >= 0.5 * target_s or rows_n >= w.M:
-            break
-        rows_n = int(min(w.M, max(rows_n * 2, rows_n * target_s / max(t, 1e-6))))
-    return {"value": 2.0 * rows_n * w.N * w.K / t / 1e12, "unit": "TFLOP/s", "cores": cores,
-            "kind": "oracle", "seconds": round(t, 3),
-            "sample": f"first {rows_n} of {w.M} rows of {w.name} (all {w.N} columns, K={w.K}), fp64"}
+        oracle.gemm_epilogue_f64(*self.args, w.M, w.N, w.K, self.dt, self.epi, rows=list(range(rows_n)))
+        return time.perf_counter() - t0
+
+    def calibrate(self, target_s: float):
+        """Rows for one call of about target_s seconds (or all rows); returns (rows, seconds)."""
+        rows_n = min(self.w.M, max(self.cores, 1))
+        while True:
+            t = self.time(rows_n)
+            if t >= 0.5 * target_s or rows_n >= self.w.M:
+                return rows_n, t
+            var = t - self.fixed_s
+            if var < 0.25 * self.fixed_s:      # the per-row part is still lost in the fixed part's noise
+                rows_n = min(self.w.M, rows_n * 4)
+                continue
+            want = int(rows_n * max(target_s - self.fixed_s, var) / var)
+            rows_n = int(min(self.w.M, max(rows_n + 1, want)))
+
+    def tflops(self, rows_n: int, t: float) -> float:
+        return 2.0 * rows_n * self.w.N * self.w.K / t / 1e12
+
+    def sample_text(self, rows_n: int, per: str = "") -> str:
+        w = self.w
+        return (f"first {rows_n} of {w.M} rows of {w.name}{per} (all {w.N} columns, K={w.K}), fp64; "
+                f"each call first decodes all of B serially ({self.fixed_s:.2f} s, a one-row call)")
+
+
+def cpu_oracle_sample(w, target_s: float):
+    """Time the oracle on a bounded sample of rows (one call of about target_s seconds)."""
+    o = OracleSample(w)
+    rows_n, t = o.calibrate(target_s)
+    return {"value": o.tflops(rows_n, t), "unit": "TFLOP/s", "cores": o.cores, "kind": "oracle",
+            "seconds": round(t, 3), "fixed_s": round(o.fixed_s, 3), "sample": o.sample_text(rows_n)}
 
 
 def run_reference(args, world, rank):
-    """Reference arm: the CPU oracle on a bounded sample per step (rank 0 only)."""
+    """Reference arm: the CPU oracle on a bounded sample per step (rank 0 only).
+    The sample is sized like the CPU-baseline leg's, capped so that the warm-up
+    and timed steps together take about two and a half minutes."""
     if rank != 0:
         return 0
-    import oracle
     w = si.WORKLOADS[args.config]
-    A, B, bias = si.make_workload(w)
-    ba, bb = si.bits(A), si.bits(B)
-    bc = si.bits(bias) if bias is not None else None
-    epi = si.EPILOGUES[w.epilogue]
-    dt = oracle.dtype_code(w.dtype)
-    cores = oracle.max_threads()
-    rows = list(range(min(w.M, args.ref_rows)))
+    o = OracleSample(w)
+    per_step = min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup))
+    rows_n, _ = o.calibrate(per_step)
     for _ in range(args.warmup):
-        oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=rows)
-    times = []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        oracle.gemm_epilogue_f64(ba, bb, bc, w.M, w.N, w.K, dt, epi, rows=rows)
-        times.append(time.perf_counter() - t0)
+        o.time(rows_n)
+    times = [o.time(rows_n) for _ in range(args.steps)]
     t = sum(times) / len(times)
-    value = 2.0 * len(rows) * w.N * w.K / t / 1e12
-    sample = f"first {len(rows)} of {w.M} rows of {w.name} per step (all {w.N} columns, K={w.K}), fp64"
+    value = o.tflops(rows_n, t)
     line = {"impl": "reference", "metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(w),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": o.cores, "kind": "oracle",
+                             "fixed_s": round(o.fixed_s, 3), "sample": o.sample_text(rows_n, " per step")},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -341,7 +368,8 @@ def run_attention_bench(args, world, rank, local):
     status = tg.tgemm_last_device_status()
     if rank != 0:
         return 0 if status == 0 else 1
-    peak, hbm, peak_kind = measured_peaks()
+    peaks = measured_peaks()
+    peak, peak_kind = peaks["tflops"], peaks["kind"]
     achieved = w.flops / (mean_ms * 1e-3) / 1e12
     line = {"metric": METRIC_ATTN, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup_done, "ms_per_step": mean_ms_max,
@@ -439,18 +467,87 @@ def launch_summary(launch_ms, t_wall, steps):
                      "max": srt[-1] * 1e3, "wall_per_step": t_wall / steps * 1e6}
 
 
-def run_tgemm_bench(args, world, rank, local):
-    import gemm_epilogue_02_gb300 as tg
-    tg.load()
-    w = si.WORKLOADS[args.config]
-    dev = torch.device("cuda", local)
+def gemm_buffers(w, dev):
+    """The workload's seeded inputs on the host and their device copies (C with
+    the workload's pitch)."""
     A, B, bias = si.make_workload(w)
     ldc = w.ldc or w.N
     Ad = A.to(dev)[:, : w.K]
     Bd = B.to(dev)[:, : w.N]
     bd = bias.to(dev) if bias is not None else None
-    Cfull = torch.empty((w.M, ldc), dtype=A.dtype, device=dev)
-    Cd = Cfull[:, : w.N]
+    Cd = torch.empty((w.M, ldc), dtype=A.dtype, device=dev)[:, : w.N]
+    return (A, B, bias), (Ad, Bd, bd, Cd)
+
+
+def check_rows(M: int) -> list:
+    """One row of every 128-row block of C (a different offset in each block),
+    plus the first and the last row."""
+    rows = {min(M - 1, b * 128 + (b * 37) % 128) for b in range((M + 127) // 128)}
+    return sorted(rows | {0, M - 1})
+
+
+def check_output(w, inputs, Cd):
+    """Compare sampled rows of the timed launch's C (every column) with the fp64
+    oracle: the method's bounds (relative Frobenius <= 2e-3, per element
+    |err| <= 1e-2 + 1e-2 |ref|), bit-exactness for integer inputs."""
+    import oracle
+    A, B, bias = inputs
+    rows = check_rows(w.M)
+    got_bits = Cd[rows].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    dt = oracle.dtype_code(w.dtype)
+    ref = oracle.gemm_epilogue_f64(si.bits(A), si.bits(B), si.bits(bias) if bias is not None else None,
+                                   w.M, w.N, w.K, dt, si.EPILOGUES[w.epilogue], rows=rows)
+    got = oracle.decode(got_bits, dt)
+    err = np.abs(got - ref)
+    frob = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-12))
+    elem = float(np.max(err / (1e-2 + 1e-2 * np.abs(ref)))) if err.size else 0.0
+    out = {"rows": len(rows), "cols": w.N, "rows_sampled": "one per 128-row block + first + last",
+           "max_abs_err": float(err.max()) if err.size else 0.0, "frobenius_rel": frob,
+           "max_err_over_elem_bound": elem, "within_bound": bool(frob <= 2e-3 and elem <= 1.0)}
+    if w.kind == "int":
+        want = oracle.round_to(ref, dt)
+        zero = (want & 0x7FFF) == 0          # +-0 compare equal (exact zero sums may carry either sign)
+        same = (got_bits == want) | (zero & ((got_bits & 0x7FFF) == 0))
+        out["bit_exact"] = bool(same.all())
+        out["within_bound"] = out["within_bound"] and out["bit_exact"]
+    return out
+
+
+def gemm_roofline(w, mean_ms, peaks, bound=None):
+    """The roofline that bounds a launch: the tensor pipe (2MNK flops at the
+    measured dense peak) or HBM (its algorithmic bytes at the measured copy
+    bandwidth), whichever takes longer; `bound` forces one.  For the skinny,
+    weight-bound shape the algorithmic bytes are B alone (the weight stream)."""
+    flops = float(w.flops)
+    skinny = w.M <= 256 and w.N * w.K >= 64 * w.M * max(w.N, w.K)
+    alg_bytes = w.K * w.N * 2 if skinny else (w.M * w.K + w.K * w.N + w.M * w.N + w.N) * 2
+    if bound is None:
+        bound = "hbm" if alg_bytes / (peaks["hbm"] * 1e9) > flops / (peaks["tflops"] * 1e12) else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": alg_bytes / (mean_ms * 1e-3) / 1e9, "peak": peaks["hbm"],
+                "unit": "GB/s", "peak_source": f"{peaks['kind']} HBM copy bandwidth",
+                "algorithmic_bytes": "B (K x N x 2 bytes): the weight stream" if skinny
+                else "A + B + C + bias, once each"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (mean_ms * 1e-3) / 1e12, "peak": peaks["tflops"],
+                "unit": "TFLOP/s", "peak_source": f"{peaks['kind']} dense bf16 burst (fp16 nominal rate is equal)"}
+        if peaks.get("tflops_sustained"):
+            roof["peak_sustained"] = peaks["tflops_sustained"]
+            roof["frac_sustained"] = roof["achieved"] / peaks["tflops_sustained"]
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof.update(kernel="tgemm_fused_kernel", algorithmic_flops_per_launch=flops,
+                algorithmic_bytes_per_launch=alg_bytes)
+    return roof
+
+
+def run_tgemm_bench(args, world, rank, local):
+    import gemm_epilogue_02_gb300 as tg
+    tg.load()
+    w = si.WORKLOADS[args.config]
+    dev = torch.device("cuda", local)
+    inputs, (Ad, Bd, bd, Cd) = gemm_buffers(w, dev)
+    A, B, bias = inputs
+    ldc = w.ldc or w.N
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
     flops = float(w.flops)
@@ -462,6 +559,8 @@ def run_tgemm_bench(args, world, rank, local):
     mean_ms, launch_stats = launch_summary(launch_ms, t_wall, args.steps)
     mean_ms_max = max_over_ranks(mean_ms, world)
     value = world * flops / (mean_ms_max * 1e-3) / 1e12
+    torch.cuda.synchronize(dev)
+    check = check_output(w, inputs, Cd) if not args.no_check else None
 
     # End to end through the host-buffer entry point (pinned host memory).
     e2e = None
@@ -489,41 +588,115 @@ def run_tgemm_bench(args, world, rank, local):
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": w.M * w.N * 2,
                "ms_per_step": e2e_ms, "steps": n_e2e, "host_memory": "pinned"}
+        del Ah, Bh, bh, Ch
+
+    # The other graded shapes, timed with the same protocol in the same run.
+    extras = {}
+    if not args.no_extras and args.config == DEFAULT_WORKLOAD:
+        extras["skinny"] = sub_record("c3", args, dev, stream, flush, world, local, check=not args.no_check)
+        extras["launch_bound"] = launch_bound_record("c0", args, dev, stream)
 
     status = tg.tgemm_last_device_status()
     if rank != 0:
         return 0 if status == 0 else 1
 
-    peak, hbm, peak_kind = measured_peaks()
-    traffic = recorded_traffic(args.config)
-    # The roofline that bounds the launch: the tensor pipe (2MNK at the measured
-    # dense peak) or HBM (A + B + C + bias once, at the measured copy bandwidth),
-    # whichever takes longer.
-    alg_bytes = (w.M * w.K + w.K * w.N + w.M * w.N + w.N) * 2
-    if alg_bytes / (hbm * 1e9) > flops / (peak * 1e12):
-        roof = {"bound": "hbm", "achieved": alg_bytes / (mean_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
-                "peak_source": f"{peak_kind} HBM copy bandwidth"}
-    else:
-        roof = {"bound": "tensor", "achieved": flops / (mean_ms * 1e-3) / 1e12, "peak": peak, "unit": "TFLOP/s",
-                "peak_source": f"{peak_kind} dense bf16 burst (fp16 nominal rate is equal)"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    peaks = measured_peaks()
+    roof = gemm_roofline(w, mean_ms, peaks)
+    roof["traffic"] = recorded_traffic(args.config)
+    clocks = clk.summary()
     line = {"metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup_done, "ms_per_step": mean_ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
             "data": "synthetic", "config": workload_config(w),
-            "roofline": dict(roof, traffic=traffic, kernel="tgemm_fused_kernel",
-                             algorithmic_flops_per_launch=flops, algorithmic_bytes_per_launch=alg_bytes),
-            "clocks": clk.summary(),
-            "gpu_launches": args.steps * (1 + (1 if (w.lda or w.K) % 8 else 0) + (1 if (w.ldb or w.N) % 8 else 0)),
+            "roofline": roof,
+            "clocks": clocks,
+            "gpu_launches": args.steps * launches_per_call(w),
             "launch_us": launch_stats,
             "device_status": tg.tgemm_status_string(status),
             "wall_s_timed_region": t_wall}
+    if clocks.get("sm_mhz"):
+        # Work per SM clock: the same launch read against the clock it ran at.
+        line["tflop_per_ghz"] = roof["achieved"] / (clocks["sm_mhz"] / 1e3) if roof["bound"] == "tensor" else None
+    if check is not None:
+        line["check"] = check
     if e2e is not None:
         line["e2e"] = e2e
+    line.update(extras)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
-    return 0 if status == 0 else 1
+    ok = status == 0 and (check is None or check["within_bound"])
+    ok = ok and all(r.get("check", {}).get("within_bound", True) for r in extras.values())
+    return 0 if ok else 1
+
+
+def launches_per_call(w) -> int:
+    """Kernels one tgemm_run call of the workload launches: the fused GEMM, plus
+    one repack per operand whose pitch is not a multiple of 8 elements."""
+    return 1 + (1 if (w.lda or w.K) % 8 else 0) + (1 if (w.ldb or w.N) % 8 else 0)
+
+
+def sub_record(name, args, dev, stream, flush, world, local, check=True):
+    """Another graded workload timed with the main line's protocol (warm-up and
+    soak, L2 flushed before each timed launch, CUDA events on the launch stream)."""
+    import gemm_epilogue_02_gb300 as tg
+    w = si.WORKLOADS[name]
+    inputs, (Ad, Bd, bd, Cd) = gemm_buffers(w, dev)
+
+    def step():
+        tg.run(Ad, Bd, bd, Cd, w.epilogue, stream=stream)
+
+    sub = argparse.Namespace(**vars(args))
+    launch_ms, t_wall, clk = timed_steps(step, flush, sub, dev, stream, world, local)
+    mean_ms, stats = launch_summary(launch_ms, t_wall, sub.steps)
+    mean_ms = max_over_ranks(mean_ms, world)
+    torch.cuda.synchronize(dev)
+    peaks = measured_peaks()
+    roof = gemm_roofline(w, mean_ms, peaks)
+    roof["traffic"] = recorded_traffic(name)
+    rec = {"workload": w.name, "config": workload_config(w), "ms_per_step": mean_ms,
+           "value": world * w.flops / (mean_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "steps": sub.steps,
+           "warmup": sub.warmup_done, "roofline": roof, "clocks": clk.summary(), "launch_us": stats,
+           "gpu_launches": sub.steps * launches_per_call(w)}
+    if check:
+        rec["check"] = check_output(w, inputs, Cd)
+    return rec
+
+
+def launch_bound_record(name, args, dev, stream, reps=1000):
+    """The launch-bound workload: `reps` back-to-back calls (no flush; its
+    operands are 256 KiB).  Reports the device time per launch (CUDA events
+    around the whole burst) and the host time per tgemm_run call."""
+    import gemm_epilogue_02_gb300 as tg
+    w = si.WORKLOADS[name]
+    _, (Ad, Bd, bd, Cd) = gemm_buffers(w, dev)
+    with torch.cuda.stream(stream):
+        for _ in range(50):
+            tg.run(Ad, Bd, bd, Cd, w.epilogue, stream=stream)
+        torch.cuda.synchronize(dev)
+        # Host cost per call while the GPU keeps up (the queue stays short).
+        t_host = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            tg.run(Ad, Bd, bd, Cd, w.epilogue, stream=stream)
+            t_host.append(time.perf_counter() - t0)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(reps):
+            tg.run(Ad, Bd, bd, Cd, w.epilogue, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    dev_us = e0.elapsed_time(e1) * 1e3 / reps
+    t_host.sort()
+    return {"workload": w.name, "config": workload_config(w) | {"l2": "not flushed (launch-bound burst)"},
+            "reps": reps, "device_us_per_launch": dev_us, "wall_us_per_call": wall / reps * 1e6,
+            "host_us_per_call_p50": t_host[len(t_host) // 2] * 1e6,
+            "host_us_per_call_p90": t_host[int(0.9 * len(t_host))] * 1e6,
+            "value": w.flops / (dev_us * 1e-6) / 1e12, "unit": "TFLOP/s",
+            "note": "python binding + C ABI; the library's own host cost is the C part of each call"}
 
 
 def main():
@@ -535,9 +708,12 @@ def main():
     ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS) + sorted(si.ATTN_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-check", action="store_true", help="skip the oracle check of the timed output")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the skinny and launch-bound sub-records of the default line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--soak", type=float, default=1.0, help="minimum seconds of warm-up steps")
-    ap.add_argument("--ref-rows", type=int, default=64, help="oracle rows per reference step")
+    ap.add_argument("--ref-rows", type=int, default=64, help="attention oracle query rows per reference step")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)          # at least 3 untimed warm-up steps
     world, rank, local = dist_setup()

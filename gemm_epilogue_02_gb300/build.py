@@ -7,6 +7,7 @@ without a GPU driver.
 """
 from __future__ import annotations
 
+import glob
 import os
 import shutil
 import subprocess
@@ -14,8 +15,8 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SRC = os.path.join(HERE, "csrc", "tgemm_api.cu")
-DEPS = [os.path.join(HERE, "csrc", f) for f in ("gemm_kernel.cuh", "ptx.cuh", "aux_kernels.cuh")] + [
-    os.path.join(ROOT, "include", "tgemm.h")]
+# Every header the translation unit includes: all of csrc/*.cuh and the C ABI.
+DEPS = sorted(glob.glob(os.path.join(HERE, "csrc", "*.cuh"))) + [os.path.join(ROOT, "include", "tgemm.h")]
 LIB = os.path.join(HERE, "libtgemm.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

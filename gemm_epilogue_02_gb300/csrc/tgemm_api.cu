@@ -10,6 +10,7 @@
 #include <cmath>
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -37,7 +38,7 @@ struct DeviceInfo {
     std::mutex mu;          // guards lazily set kernel attributes
     unsigned attr_set = 0;  // bit per kernel configuration
     unsigned attn_attr_set = 0;   // bit per attention kernel (format x causal)
-    int max_clusters[3] = {0, 0, 0};   // co-resident clusters per CTA-group size
+    int max_clusters[32] = {};         // co-resident clusters per CTA-pair kernel (by attribute bit)
     cudaStream_t copy_in = nullptr;    // tgemm_run_host: host->device copies
     cudaStream_t copy_out = nullptr;   // tgemm_run_host: device->host copies
 };
@@ -101,10 +102,27 @@ struct Range {
     uintptr_t lo, hi;
 };
 
+// Byte extent of a [rows x width] 16-bit matrix with pitch ld; false when it
+// does not fit in 2^62 bytes (no valid allocation is that large).
+bool extent_bytes(int64_t rows, int64_t ld, int64_t width, int64_t *bytes) {
+    if (rows <= 0 || width <= 0) {
+        *bytes = 0;
+        return true;
+    }
+    int64_t e = 0;
+    if (__builtin_mul_overflow(rows - 1, ld, &e) || __builtin_add_overflow(e, width, &e) ||
+        e > (int64_t(1) << 61))
+        return false;
+    *bytes = e * 2;
+    return true;
+}
+
+// Byte range of a matrix whose extent_bytes() was checked.
 Range span(const void *p, int64_t rows, int64_t ld, int64_t width) {
     const uintptr_t b = reinterpret_cast<uintptr_t>(p);
-    if (rows <= 0 || width <= 0) return {b, b};
-    return {b, b + static_cast<uintptr_t>(((rows - 1) * ld + width) * 2)};
+    int64_t bytes = 0;
+    extent_bytes(rows, ld, width, &bytes);
+    return {b, b + static_cast<uintptr_t>(bytes)};
 }
 
 bool overlaps(Range a, Range b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
@@ -145,6 +163,10 @@ tgemm_status validate(const void *A, const void *B, const void *bias, const void
     if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))) ||
         (use_bias && !aligned16(bias)))
         return TGEMM_ERR_ALIGNMENT;
+    int64_t bytes = 0;
+    if (!extent_bytes(M, ldc, N, &bytes) ||
+        (K > 0 && (!extent_bytes(a_rows, lda, a_cols, &bytes) || !extent_bytes(b_rows, ldb, b_cols, &bytes))))
+        return TGEMM_ERR_INVALID_ARG;
     const Range rc = span(C, M, ldc, N);
     if (K > 0 && (overlaps(rc, span(A, a_rows, lda, a_cols)) || overlaps(rc, span(B, b_rows, ldb, b_cols))))
         return TGEMM_ERR_ALIAS;
@@ -335,11 +357,11 @@ cudaError_t launch_fused(DeviceInfo *d, unsigned bit, const CUtensorMap &ta, con
                     cudaGetLastError();
                     clusters = d->num_sms / CG;
                 }
-                d->max_clusters[CG] = clusters;
+                d->max_clusters[__builtin_ctz(bit)] = clusters;
             }
             d->attr_set |= bit;
         }
-        if (CG == 2) max_groups = d->max_clusters[CG];
+        if (CG == 2) max_groups = d->max_clusters[__builtin_ctz(bit)];
     }
 #ifdef TGEMM_TRACE
     // Trace builds: run the persistent loop on fewer groups (timeline studies).
@@ -606,7 +628,16 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     p.narrow_first = static_cast<int>(plan.narrow_first);
     p.narrow_parts = plan.narrow_parts;
     if (const char *e = std::getenv("TGEMM_TEST_STALL"))
-        if (std::atoi(e) != 0) p.test_extra_tx = 16;   // testing only: see KParams::test_extra_tx
+        if (std::atoi(e) != 0) {
+            // Testing only (see KParams::test_extra_tx): every call with it set
+            // stalls for the wait limit and fails, so say so loudly, once.
+            static std::once_flag warned;
+            std::call_once(warned, []() {
+                std::fprintf(stderr, "tgemm: TGEMM_TEST_STALL is set: GEMM calls will time out on purpose "
+                                     "(testing the failure path only)\n");
+            });
+            p.test_extra_tx = 16;
+        }
     if (p.split_k > 1) {
         const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn) - plan.split_first;
         const int64_t pbytes = tiles * p.split_k * partial_floats_per_unit(cfg) * 4;

@@ -192,8 +192,14 @@ tgemm_status tgemm_run_host(const void *A_host, const void *B_host, const void *
  * the device address of the array once; make that first call before any
  * stream capture.
  *
- * Arguments, layout, results and the other error codes are those of
- * tgemm_run, and the results are identical to tgemm_run's.
+ * Arguments, layout and the other error codes are those of tgemm_run.
+ * Results: this variant never splits the k loop (the fp32 partial sums would
+ * need scratch), while tgemm_run splits it for problems with few output tiles
+ * and may split the tiles of a last, partial wave.  The two therefore agree
+ * bit for bit wherever tgemm_run's plan has no k split (tgemm_plan reports
+ * split_k == 1) and whenever every partial sum is exact (small-integer
+ * inputs); otherwise both are within the same error bound of the exact
+ * result and may differ in the last bits.
  */
 #define TGEMM_NOALLOC_SCRATCH_BYTES (64ull << 20)
 tgemm_status tgemm_run_noalloc(const void *A, const void *B, const void *bias, void *C,

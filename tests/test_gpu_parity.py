@@ -25,10 +25,13 @@ pytestmark = pytest.mark.gpu
 
 
 def sample_rows(M, n=48, seed=0):
+    """Fixed edge rows, n random rows, and one row of every 128-row block (a
+    different offset in each), so that every output tile has a checked row."""
     rng = np.random.default_rng(seed)
     fixed = [0, 1, 127, 128, 129, M // 2, M - 129, M - 128, M - 2, M - 1]
     rows = set(r for r in fixed if 0 <= r < M)
     rows |= set(rng.choice(M, size=min(n, M), replace=False).tolist())
+    rows |= {min(M - 1, b * 128 + int(rng.integers(128))) for b in range((M + 127) // 128)}
     return sorted(rows)
 
 

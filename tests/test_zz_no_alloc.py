@@ -24,8 +24,8 @@ import pytest
 import torch
 
 import seeded_inputs as si
-from gpu_helpers import (SENTINEL, TINY, U_OUT, alloc_c, assert_close, c_bits, decode, magnitude, oracle_ref,
-                         to_device_pitched)
+from gpu_helpers import (SENTINEL, TINY, U_OUT, alloc_c, assert_bit_exact, assert_close, c_bits, decode, magnitude,
+                         oracle_ref, to_device_pitched)
 
 pytestmark = pytest.mark.gpu
 
@@ -84,6 +84,30 @@ def test_noalloc_matches_run_on_consecutive_calls(cuda_lib):
             bound = 2 * (U_OUT[dt] * np.abs(ref) + (1 + U_OUT[dt]) * gamma * mag + TINY[dt])
             diff = np.abs(decode(got[:, :N], dt) - decode(want[:, :N], dt))
             assert (diff <= bound).all(), what
+    assert cuda_lib.tgemm_last_device_status() == 0
+
+
+def test_noalloc_integer_inputs_bit_exact_on_a_few_tile_shape(cuda_lib):
+    """A decode-like shape (few output tiles, long k loop) with an unaligned
+    pitch of A: tgemm_run splits its k loop across CTAs, this variant never
+    does, so their summation orders differ; with small-integer inputs every
+    partial sum is exact, so both must equal the oracle's rounding bit for bit
+    (and hence each other), on two calls in a row."""
+    M, N, K, dt, epi, lda = 128, 1024, 4096, "fp16", "bias_relu", 4100
+    plan = cuda_lib.tgemm_plan(M, N, K, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["split_k"] > 1            # the two entry points really take different plans
+    A, B, bias = si.make_inputs(M, N, K, dt, 41, kind="int", lda=lda)
+    Ad, Bd, bd = to_device_pitched(A, K), B.to("cuda"), bias.to("cuda")
+    want = oracle_ref((A, B, bias), M, N, K, dt, epi)
+    Cr = alloc_c(M, N, N, dt)
+    assert call(cuda_lib.tgemm_run, Ad, Bd, bd, Cr, M, N, K, dt, epi) == 0
+    for rep in range(2):
+        Cn = alloc_c(M, N, N, dt)
+        assert call(cuda_lib.tgemm_run_noalloc, Ad, Bd, bd, Cn, M, N, K, dt, epi) == 0
+        torch.cuda.synchronize()
+        got = c_bits(Cn, M, N)
+        assert_bit_exact(got, want, dt, f"noalloc int call {rep + 1}")
+        assert (got == c_bits(Cr, M, N)).all(), f"noalloc and tgemm_run differ on call {rep + 1}"
     assert cuda_lib.tgemm_last_device_status() == 0
 
 
