@@ -6,37 +6,74 @@
 
 namespace tgemm {
 
+// One 16-byte-aligned block of the source array at byte offset `off`: a
+// single 16-byte load when the block lies inside the `span` bytes the matrix
+// covers, else element by element (zero outside), so that no byte beyond the
+// matrix is read.
+__device__ __forceinline__ uint4 load_block16(const unsigned char *__restrict__ base, long long off,
+                                              long long span) {
+    if (off + 16 <= span) return __ldg(reinterpret_cast<const uint4 *>(base + off));
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const long long e = off + 4 * i;
+        const uint32_t lo = (e + 2 <= span) ? __ldg(reinterpret_cast<const uint16_t *>(base + e)) : 0u;
+        const uint32_t hi = (e + 4 <= span) ? __ldg(reinterpret_cast<const uint16_t *>(base + e + 2)) : 0u;
+        w[i] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Bytes [o, o + 16) of the 32 bytes lo:hi (little-endian), o even, 0 < o < 16.
+__device__ __forceinline__ uint4 shift_bytes16(const uint4 &lo, const uint4 &hi, int o) {
+    uint32_t a0, a1, a2, a3, a4;
+    switch (o >> 2) {       // whole words first
+        case 0: a0 = lo.x; a1 = lo.y; a2 = lo.z; a3 = lo.w; a4 = hi.x; break;
+        case 1: a0 = lo.y; a1 = lo.z; a2 = lo.w; a3 = hi.x; a4 = hi.y; break;
+        case 2: a0 = lo.z; a1 = lo.w; a2 = hi.x; a3 = hi.y; a4 = hi.z; break;
+        default: a0 = lo.w; a1 = hi.x; a2 = hi.y; a3 = hi.z; a4 = hi.w; break;
+    }
+    if (o & 2)              // then half a word
+        return make_uint4(__funnelshift_r(a0, a1, 16), __funnelshift_r(a1, a2, 16), __funnelshift_r(a2, a3, 16),
+                          __funnelshift_r(a3, a4, 16));
+    return make_uint4(a0, a1, a2, a3);
+}
+
 // Copy a [rows x cols] 16-bit matrix from pitch `lds` to pitch `ldd` (ldd a
-// multiple of 8 elements, dst 16-byte aligned), so that tensor-memory-access
-// copies, which need 16-byte row strides, can read an operand whose own pitch
-// is unaligned.  Each thread writes one 16-byte vector of a destination row
-// (8 elements) from 8 coalesced 2-byte source reads; blockIdx.y walks rows.
-// HBM-bound: 2 x rows x cols x 2 bytes.
+// multiple of 8 elements, dst 16-byte aligned; src 16-byte aligned), so that
+// tensor-memory-access copies, which need 16-byte row strides, can read an
+// operand whose own pitch is unaligned.  A source row starts o bytes past a
+// 16-byte boundary (o even); each thread writes one 16-byte vector of a
+// destination row (8 elements) from the two aligned 16-byte source blocks it
+// straddles, shifted by o bytes.  The destination's pitch padding of the last
+// vector is written as zero.  HBM-bound: 2 x rows x cols x 2 bytes.
 __global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t *__restrict__ src, long long lds,
                                                           uint16_t *__restrict__ dst, long long ldd,
                                                           long long rows, long long cols) {
     const long long vec_per_row = (cols + 7) / 8;
+    const unsigned char *base = reinterpret_cast<const unsigned char *>(src);
+    const long long span = ((rows - 1) * lds + cols) * 2;   // bytes of src the matrix covers
     for (long long r = blockIdx.y; r < rows; r += gridDim.y) {
-        const uint16_t *s = src + r * lds;
+        const long long row_off = r * lds * 2;
+        const int o = static_cast<int>(row_off & 15);
+        const long long al = row_off - o;
         uint4 *d = reinterpret_cast<uint4 *>(dst + r * ldd);
         for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < vec_per_row;
              v += static_cast<long long>(gridDim.x) * blockDim.x) {
-            const long long c0 = v * 8;
-            uint32_t w[4];
-            if (c0 + 8 <= cols) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    w[i] = static_cast<uint32_t>(__ldg(s + c0 + 2 * i)) |
-                           (static_cast<uint32_t>(__ldg(s + c0 + 2 * i + 1)) << 16);
-            } else {
+            const uint4 lo = load_block16(base, al + 16 * v, span);
+            uint4 out = lo;
+            if (o != 0) out = shift_bytes16(lo, load_block16(base, al + 16 * v + 16, span), o);
+            const long long valid = cols - 8 * v;   // elements of this vector inside the row (>= 1)
+            if (valid < 8) {
+                uint32_t w[4] = {out.x, out.y, out.z, out.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint32_t lo = (c0 + 2 * i < cols) ? __ldg(s + c0 + 2 * i) : 0u;
-                    const uint32_t hi = (c0 + 2 * i + 1 < cols) ? __ldg(s + c0 + 2 * i + 1) : 0u;
-                    w[i] = lo | (hi << 16);
+                    if (2 * i >= valid) w[i] = 0u;
+                    else if (2 * i + 1 >= valid) w[i] &= 0xFFFFu;
                 }
+                out = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            d[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            d[v] = out;
         }
     }
 }
