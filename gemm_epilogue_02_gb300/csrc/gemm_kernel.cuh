@@ -342,13 +342,21 @@ __device__ __forceinline__ void epi_math32(const uint32_t (&r)[32], const uint4 
 // activation (epi_math32<MODE >= 3, MODE % 3>), which keeps the kernel's code
 // small (the epilogue warps otherwise carry all six bodies and stall on
 // instruction fetch); -1: chosen at run time.
-template <int BN, int STAGES, int CG, int KSUB, int MODE = -1>
+// MC = 2 (CTA pairs only): a cluster holds two pairs stacked in M, whose tile
+// is (256 * 2) x BN.  The two CTAs of equal rank in the two pairs need the
+// same BN/2 columns of B: each loads one of their two 64-column sub-tiles and
+// multicasts it to both, so every CTA reads half of its B slice from L2 (a
+// quarter less operand traffic per SM).  A stage is refilled only once both
+// pairs' MMAs are done with it (its empty barrier counts one commit of each).
+template <int BN, int STAGES, int CG, int KSUB, int MODE = -1, int MC = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     tgemm_fused_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmB2,
                        const __grid_constant__ CUtensorMap tmC, const KParams p) {
     using L = Smem<BN, STAGES, CG>;
     static_assert(KSUB >= 1 && KSUB <= STAGES, "a slot fits the ring");
+    static_assert(MC == 1 || (MC == 2 && CG == 2 && L::kBSub == 2), "multicast pairs share two B sub-tiles");
+    constexpr int kCluster = CG * MC;         // CTAs per cluster (one work unit)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
@@ -376,20 +384,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.trace[blockIdx.x * 64 + 5] = clock64();
     }
 #endif
-    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-    const int group_id = (CG == 2) ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-    const int num_groups = (CG == 2) ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
-    // Barriers that rank 0 owns for the whole group, as shared::cluster addresses.
-    auto leader_full = [&](int s) { return (CG == 2) ? mapa_shared(full_bar(s), 0) : full_bar(s); };
-    auto leader_tempty = [&](int a) { return (CG == 2) ? mapa_shared(tempty_bar(a), 0) : tempty_bar(a); };
+    // crank: rank in the cluster; rank: rank within the CTA pair; pp: the pair
+    // (0 .. MC-1); lead: cluster rank of the pair's even CTA, which owns the
+    // pair's full and accumulator barriers and issues its MMAs.
+    const uint32_t crank = (kCluster > 1) ? cluster_ctarank() : 0u;
+    const uint32_t rank = crank % CG;
+    const uint32_t pp = crank / CG;
+    const uint32_t lead = crank - rank;
+    const int group_id = (kCluster > 1) ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int num_groups = (kCluster > 1) ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
+    // Barriers that the pair's even CTA owns for the pair, as shared::cluster addresses.
+    auto leader_full = [&](int s) { return (CG == 2) ? mapa_shared(full_bar(s), lead) : full_bar(s); };
+    auto leader_tempty = [&](int a) { return (CG == 2) ? mapa_shared(tempty_bar(a), lead) : tempty_bar(a); };
+    // Rows of A (and C) per unit, and this CTA's first row within the unit.
+    constexpr int kUnitRows = kBM * kCluster;
+    const int cta_row0 = static_cast<int>(pp) * (kBM * CG) + static_cast<int>(rank) * kBM;
 
     if (threadIdx.x == 0) {
         // Full barriers: one per slot in flight (a slot may hold a single k-block,
-        // so as many as stages); rank 0's expect-tx arrival carries the bytes of
-        // the whole group.  Empty barriers: one per stage, freed k-block by k-block.
+        // so as many as stages); the pair's even CTA's expect-tx arrival carries
+        // the bytes of the whole pair.  Empty barriers: one per stage, freed
+        // k-block by k-block (by the MMA commit of each pair whose operands the
+        // stage's copies feed: MC of them).
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), MC);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -406,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.b_3d) prefetch_tmap(&tmB2);
         if (p.tma_store) prefetch_tmap(&tmC);
     }
-    if constexpr (CG == 2) cluster_sync();       // the peer is running and its barriers exist
+    if constexpr (kCluster > 1) cluster_sync();  // the peers are running and their barriers exist
     if (warp == 1) {
         tmem_alloc<CG>(smem_u32(tmem_holder), L::kTmemCols);
         tmem_relinquish<CG>();
@@ -432,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int m_blk, n_blk;
                 tile_coords(w.t, p, m_blk, n_blk);
                 const bool narrow = w.width != BN;
-                const int a_row = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM;
+                const int a_row = m_blk * kUnitRows + cta_row0;
                 // Each CTA of the group holds width / CG columns of the unit's B.
                 const int b_col = n_blk * BN + w.col0 + static_cast<int>(rank) * (w.width / CG);
                 const int b_sub = narrow ? (w.width / CG) / 64 : L::kBSub;
@@ -478,7 +497,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int j = 0; j < kBM / 64; ++j)
                                 load(a_dst + j * (kBK * 128), &tmA, a_row + j * 64, k0);
                         }
-                        if (p.b_3d && !narrow) {
+                        if (MC == 2 && !narrow) {
+                            // This CTA's B slice is shared with the same rank of the other
+                            // pair: each loads one of its two 64-column (or, B stored
+                            // [N, K], 64-row) sub-tiles and multicasts it to both.
+                            const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
+                            const int sub0 = b_col + static_cast<int>(pp) * 64;
+                            if (!p.b_kmajor)
+                                tma_load_2d_pair_mc(b_dst + pp * (kBK * 128), p.b_3d ? &tmB2 : &tmB, fb, sub0, k0, mask);
+                            else
+                                tma_load_2d_pair_mc(b_dst + pp * (64 * 128), &tmB2, fb, k0, sub0, mask);
+                        } else if (p.b_3d && !narrow) {
                             // B [K, N] viewed as (64 columns, K rows, column chunks): one box
                             // holds the kBSub 64-column sub-tiles of 64 k-rows (MN-major),
                             // laid out as the 2-D copies would place them.
@@ -525,6 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // many cycles per MMA.
         if (rank == 0) {
             const bool issuer = elect_one_sync() != 0u;
+            // Commit targets: a stage's empty barrier in every CTA whose copies feed
+            // it (the whole cluster), the accumulator barrier in this pair's CTAs.
+            const uint16_t kEmptyMask = static_cast<uint16_t>((1u << kCluster) - 1u);
+            const uint16_t kPairMask = static_cast<uint16_t>(3u << (CG * pp));
             int stage = 0, fbar = 0;    // ring position, as in the producer
             uint32_t fphase = 0;
             int acc = 0;
@@ -569,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int k = 0; k < kBK / kUmmaK; ++k)
                                 mma_f16_ss<CG>(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc,
                                                (i == 0 && k == 0) ? accumulate : 1u);
-                            mma_commit<CG>(empty_bar(st));      // frees the stage once read
+                            mma_commit<CG>(empty_bar(st), kEmptyMask);   // frees the stage once read
                         }
                     }
                     stage += nkb;
@@ -579,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (++fbar == STAGES) { fbar = 0; fphase ^= 1u; }
                 }
                 if (!ok) break;
-                if (issuer) mma_commit<CG>(tfull_bar(acc));   // accumulator ready for the epilogue
+                if (issuer) mma_commit<CG>(tfull_bar(acc), kPairMask);   // accumulator ready for the epilogue
                 if (tile_i < 8) TGEMM_STAMP(9 + 4 * tile_i);
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
@@ -658,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (warp == 2 && lane == 0 && tile_i < 8) TGEMM_STAMP(10 + 4 * tile_i);
             TGEMM_EPI_STAMP(0);
-            const int m0 = m_blk * (kBM * CG) + static_cast<int>(rank) * kBM + q * 32;
+            const int m0 = m_blk * kUnitRows + cta_row0 + q * 32;
             const int n_tile = n_blk * BN + w.col0;     // accumulator column 0 is C column n_tile
             // Only chunks / rows that intersect C are read out and stored (no
             // store is ever issued at a coordinate outside the tensor).
@@ -765,11 +798,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Split-K: this warp's fp32 partial region of unit (t, range); float4 g
             // of lane l's 32 values of sub-chunk `sub` sits at sub*1024 + g*128 + l*4.
             constexpr int kMaxSub = L::kBiasCols / 32;
-            // Regions and counters are per (tile, range, CTA of the group, epilogue warp).
-            const int wid = static_cast<int>(rank) * kEpiWarps + ew;
+            // Regions and counters are per (tile, range, CTA of the cluster, epilogue warp).
+            const int wid = static_cast<int>(crank) * kEpiWarps + ew;
             const int ts = t - p.split_first;     // index among the split tiles
             auto region = [&](int range) {
-                return p.partials + ((static_cast<long long>(ts) * p.split_k + range) * (CG * kEpiWarps) + wid) *
+                return p.partials + ((static_cast<long long>(ts) * p.split_k + range) * (kCluster * kEpiWarps) + wid) *
                                         (kMaxSub * 1024);
             };
             if (split >= 0) {
@@ -803,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(41);
                     unsigned int arrived = 0;
-                    if (lane == 0) arrived = atomicAdd(p.counters + ts * (CG * kEpiWarps) + wid, 1u);
+                    if (lane == 0) arrived = atomicAdd(p.counters + ts * (kCluster * kEpiWarps) + wid, 1u);
                     arrived = __shfl_sync(0xffffffffu, arrived, 0);
 #ifdef TGEMM_TRACE
                     if (warp == 2 && lane == 0 && tile_i == 0 && blockIdx.x < 160) {
@@ -861,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp();
                         if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(44);
-                        if (lane == 0) p.counters[ts * (CG * kEpiWarps) + wid] = 0u;   // ready for the next launch
+                        if (lane == 0) p.counters[ts * (kCluster * kEpiWarps) + wid] = 0u;   // ready for the next launch
                     }
                 }
             } else if (n_sub == 0) {
@@ -908,10 +941,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) TGEMM_STAMP(2);
-    if constexpr (CG == 2) cluster_sync();       // both CTAs are done with TMEM and remote barriers
+    if constexpr (kCluster > 1) cluster_sync();  // all CTAs are done with TMEM and remote barriers
     tc_fence_after();
     if (warp == 1) tmem_dealloc<CG>(tmem_base, L::kTmemCols);
-    if constexpr (CG == 2) cluster_sync();       // the peer stays resident until both have freed TMEM
+    if constexpr (kCluster > 1) cluster_sync();  // the peers stay resident until all have freed TMEM
     if (threadIdx.x == 0) TGEMM_STAMP(3);
 #ifdef TGEMM_TRACE
     if (threadIdx.x == 0 && blockIdx.x < 160) p.trace[blockIdx.x * 64 + 6] = clock64();

@@ -134,6 +134,20 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// The pair load with cluster multicast: the box lands at offset `dst` in the
+// shared memory of every CTA whose cluster rank is set in `mask`, and each
+// destination's completion bytes go to the barrier at `bar`'s offset in the
+// even CTA of that destination's pair (`bar` is given as the issuing pair's
+// even-CTA barrier).
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                                    int32_t x, int32_t y, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
 // 3-D tiled loads (x innermost), for boxes that gather several 64-column
 // sub-tiles of one operand in a single copy.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
@@ -278,9 +292,10 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint
 
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.  CG = 2: the arrival goes to the barrier at the same
-// offset in both CTAs of the pair.
+// offset in every CTA of the cluster whose rank is set in `mask` (by default
+// the two CTAs of a pair that is alone in its cluster).
 template <int CG>
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
+__device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t mask = 3) {
     if constexpr (CG == 1)
         asm volatile(
             "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -289,7 +304,7 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         asm volatile(
             "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
             " [%0], %1;" ::"r"(bar),
-            "h"(static_cast<uint16_t>(3))
+            "h"(mask)
             : "memory");
 }
 

@@ -244,13 +244,17 @@ bool make_map_b3d(CUtensorMap *m, const void *base, int64_t K, int64_t N, int64_
 }
 
 // ---------------------------------------------------------------- configs
-// A configuration: C tile = (128 * cg) x bn, `stages` ring stages, cg CTAs per tile.
+// A configuration: C tile = (128 * cg * mc) x bn, `stages` ring stages, cg
+// CTAs per MMA (a pair when 2), mc pairs per cluster sharing B by multicast.
 struct Cfg {
     int bn;
     int stages;
     int cg;
     int bit;
+    int mc = 1;
     int cw() const { return (bn % 64 == 0) ? 64 : 32; }   // epilogue chunk / C box width (the kernel's kCW)
+    int ctas() const { return cg * mc; }                  // CTAs per tile (a cluster when > 1)
+    int rows() const { return kBM * cg * mc; }            // rows of C per tile
 };
 constexpr Cfg kCfg256 = {256, 4, 1, 1};
 constexpr Cfg kCfg192 = {192, 4, 1, 32};
@@ -259,6 +263,7 @@ constexpr Cfg kCfg64 = {64, 8, 1, 4};
 constexpr Cfg kCfg256x2 = {256, 6, 2, 8};
 constexpr Cfg kCfg224x2 = {224, 6, 2, 64};
 constexpr Cfg kCfg128x2 = {128, 8, 2, 16};
+constexpr Cfg kCfg256x4 = {256, 6, 2, 8192, 2};   // two 256 x 256 pairs sharing B: 512 x 256 tiles
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -292,7 +297,9 @@ double effective_waves(const Cfg &cfg, int64_t tiles, int64_t groups) {
 // effective waves x width x a relative cost per column (narrow single-CTA tiles
 // re-read A from shared memory more often, and a 224-wide pair tile runs at
 // the speed of a 256-wide one; measured on the 8192^3 workload).  CTA pairs
-// are preferred whenever their tiles fill every SM pair at least once.
+// are preferred whenever their tiles fill every SM pair at least once, and
+// clusters of two pairs sharing B whenever their 512 x 256 tiles fill every
+// cluster at least once (a quarter less operand traffic from L2 per SM).
 Cfg choose_config(int64_t M, int64_t N, int64_t K, int num_sms) {
     if (const char *f = std::getenv("TGEMM_FORCE_CFG")) {
         const std::string v(f);
@@ -303,16 +310,20 @@ Cfg choose_config(int64_t M, int64_t N, int64_t K, int num_sms) {
         if (v == "256x2") return kCfg256x2;
         if (v == "224x2") return kCfg224x2;
         if (v == "128x2") return kCfg128x2;
+        if (v == "256x4") return kCfg256x4;
     }
     struct Cand { Cfg cfg; double per_col; };
     (void)K;
     const int pairs = num_sms / 2;
     if (M > kBM && cdiv(M, 2 * kBM) * cdiv(N, 256) >= pairs) {
-        const Cand cands[2] = {{kCfg256x2, 1.0}, {kCfg224x2, 256.0 / 224.0}};
+        const bool shared_b = M > 2 * kBM && cdiv(M, 4 * kBM) * cdiv(N, 256) >= num_sms / 4;
+        const Cand cands[3] = {{kCfg256x4, 1.0}, {kCfg256x2, 1.0}, {kCfg224x2, 256.0 / 224.0}};
         Cfg best = kCfg256x2;
         double best_cost = 1e300;
         for (const Cand &c : cands) {
-            const double cost = effective_waves(c.cfg, cdiv(M, 2 * kBM) * cdiv(N, c.cfg.bn), pairs) * c.cfg.bn * c.per_col;
+            if (c.cfg.mc == 2 && !shared_b) continue;
+            const int64_t tiles = cdiv(M, c.cfg.rows()) * cdiv(N, c.cfg.bn);
+            const double cost = effective_waves(c.cfg, tiles, num_sms / c.cfg.ctas()) * c.cfg.bn * c.per_col;
             if (cost < best_cost - 1e-9) { best_cost = cost; best = c.cfg; }
         }
         return best;
@@ -327,11 +338,12 @@ Cfg choose_config(int64_t M, int64_t N, int64_t K, int num_sms) {
     return best;
 }
 
-template <int BN, int ST, int CG, int KSUB, int MODE = -1>
+template <int BN, int ST, int CG, int KSUB, int MODE = -1, int MC = 1>
 cudaError_t launch_fused(DeviceInfo *d, unsigned bit, const CUtensorMap &ta, const CUtensorMap &tb,
                          const CUtensorMap &tb2, const CUtensorMap &tc, const KParams &p, int64_t tiles, cudaStream_t s) {
     using L = Smem<BN, ST, CG>;
-    auto kernel = tgemm_fused_kernel<BN, ST, CG, KSUB, MODE>;
+    auto kernel = tgemm_fused_kernel<BN, ST, CG, KSUB, MODE, MC>;
+    constexpr int kCl = CG * MC;   // CTAs per cluster
     int max_groups = d->num_sms;
     {
         std::lock_guard<std::mutex> g(d->mu);
@@ -339,15 +351,15 @@ cudaError_t launch_fused(DeviceInfo *d, unsigned bit, const CUtensorMap &ta, con
             cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  L::kDynamicBytes);
             if (e != cudaSuccess) return e;
-            if (CG == 2) {
+            if (kCl > 1) {
                 cudaLaunchConfig_t qc;
                 std::memset(&qc, 0, sizeof(qc));
                 cudaLaunchAttribute qa[1];
                 qa[0].id = cudaLaunchAttributeClusterDimension;
-                qa[0].val.clusterDim.x = CG;
+                qa[0].val.clusterDim.x = kCl;
                 qa[0].val.clusterDim.y = 1;
                 qa[0].val.clusterDim.z = 1;
-                qc.gridDim = dim3(CG * (d->num_sms / CG));
+                qc.gridDim = dim3(kCl * (d->num_sms / kCl));
                 qc.blockDim = dim3(kThreads);
                 qc.dynamicSmemBytes = L::kDynamicBytes;
                 qc.attrs = qa;
@@ -355,20 +367,20 @@ cudaError_t launch_fused(DeviceInfo *d, unsigned bit, const CUtensorMap &ta, con
                 int clusters = 0;
                 if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &qc) != cudaSuccess || clusters <= 0) {
                     cudaGetLastError();
-                    clusters = d->num_sms / CG;
+                    clusters = d->num_sms / kCl;
                 }
                 d->max_clusters[__builtin_ctz(bit)] = clusters;
             }
             d->attr_set |= bit;
         }
-        if (CG == 2) max_groups = d->max_clusters[__builtin_ctz(bit)];
+        if (kCl > 1) max_groups = d->max_clusters[__builtin_ctz(bit)];
     }
 #ifdef TGEMM_TRACE
     // Trace builds: run the persistent loop on fewer groups (timeline studies).
     if (const char *g = std::getenv("TGEMM_TRACE_MAX_GROUPS")) max_groups = std::max(1, std::min(max_groups, std::atoi(g)));
 #endif
     const int groups = static_cast<int>(std::min<int64_t>(tiles, max_groups));
-    if (CG == 1) {
+    if (kCl == 1) {
         kernel<<<groups, kThreads, L::kDynamicBytes, s>>>(ta, tb, tb2, tc, p);
         return cudaGetLastError();
     }
@@ -376,10 +388,10 @@ cudaError_t launch_fused(DeviceInfo *d, unsigned bit, const CUtensorMap &ta, con
     std::memset(&lc, 0, sizeof(lc));
     cudaLaunchAttribute la[1];
     la[0].id = cudaLaunchAttributeClusterDimension;
-    la[0].val.clusterDim.x = CG;
+    la[0].val.clusterDim.x = kCl;
     la[0].val.clusterDim.y = 1;
     la[0].val.clusterDim.z = 1;
-    lc.gridDim = dim3(CG * groups);
+    lc.gridDim = dim3(kCl * groups);
     lc.blockDim = dim3(kThreads);
     lc.dynamicSmemBytes = L::kDynamicBytes;
     lc.stream = s;
@@ -396,8 +408,8 @@ cudaError_t launch_fused(DeviceInfo *d, unsigned bit, const CUtensorMap &ta, con
 // (CTA pairs: g = 8): 970 MB of DRAM reads per launch against 1181 MB with
 // g = 16, at the same time.
 int group_rows(const Cfg &cfg, int num_sms) {
-    const double groups = static_cast<double>(cfg.cg == 2 ? num_sms / 2 : num_sms);
-    const int g = static_cast<int>(std::lround(std::sqrt(groups * cfg.bn / (kBM * cfg.cg))));
+    const double groups = static_cast<double>(num_sms / cfg.ctas());
+    const int g = static_cast<int>(std::lround(std::sqrt(groups * cfg.bn / cfg.rows())));
     return std::max(1, g);
 }
 
@@ -410,7 +422,7 @@ int64_t count_units(int64_t tiles, int split_k, int64_t split_first, int64_t nar
 // Fills the tile counts and instruction descriptor for `cfg` and launches.
 cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, const CUtensorMap &tb,
                           const CUtensorMap &tb2, const CUtensorMap &tc, KParams p, cudaStream_t s, bool bf16) {
-    p.num_m = static_cast<int>(cdiv(p.M, kBM * cfg.cg));
+    p.num_m = static_cast<int>(cdiv(p.M, cfg.rows()));
     p.num_n = static_cast<int>(cdiv(p.N, cfg.bn));
     p.num_kb = static_cast<int>(cdiv(p.K, kBK));
     const int64_t tiles = static_cast<int64_t>(p.num_m) * p.num_n;
@@ -457,6 +469,16 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
                 default: return launch_fused<256, 6, 2, 2, 5>(d, 128u << 5, ta, tb, tb2, tc, p, units, s);
             }
         case 16: return launch_fused<128, 8, 2, 2>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
+        case 8192:
+            // Two pairs sharing B: one kernel per format x activation, as above.
+            switch ((bf16 ? 3 : 0) + p.act) {
+                case 0: return launch_fused<256, 6, 2, 2, 0, 2>(d, 8192u << 0, ta, tb, tb2, tc, p, units, s);
+                case 1: return launch_fused<256, 6, 2, 2, 1, 2>(d, 8192u << 1, ta, tb, tb2, tc, p, units, s);
+                case 2: return launch_fused<256, 6, 2, 2, 2, 2>(d, 8192u << 2, ta, tb, tb2, tc, p, units, s);
+                case 3: return launch_fused<256, 6, 2, 2, 3, 2>(d, 8192u << 3, ta, tb, tb2, tc, p, units, s);
+                case 4: return launch_fused<256, 6, 2, 2, 4, 2>(d, 8192u << 4, ta, tb, tb2, tc, p, units, s);
+                default: return launch_fused<256, 6, 2, 2, 5, 2>(d, 8192u << 5, ta, tb, tb2, tc, p, units, s);
+            }
         case 32: return launch_fused<192, 4, 1, 1>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
         default: return launch_fused<224, 6, 2, 2>(d, cfg.bit, ta, tb, tb2, tc, p, units, s);
     }
@@ -493,9 +515,13 @@ bool encode_maps(const Cfg &cfg, const void *a, int64_t lda, int ta, const void 
         (b3d || (tb ? make_map(tmb, b, N, K, ldb, kBK, static_cast<uint32_t>(bcols), bf16)
                     : make_map(tmb, b, K, N, ldb, 64, kBK, bf16))) &&
         (!tma_store || make_map(tmc, C, M, N, ldc, static_cast<uint32_t>(cfg.cw()), 32, bf16));
-    // The 2-D map of B [K, N] for narrow units when tmB is the 3-D view.
-    const bool ok2 = !b3d || make_map(tmb2, b, K, N, ldb, 64, kBK, bf16);
-    if (!b3d) std::memcpy(tmb2, tmb, sizeof(*tmb));
+    // The 2-D map of B [K, N] for narrow units (and shared sub-tiles) when tmB
+    // is the 3-D view; with B stored [N, K] and two pairs sharing B, a map of
+    // 64-row boxes (each pair loads one of a CTA's two 64-row sub-tiles).
+    bool ok2 = true;
+    if (b3d) ok2 = make_map(tmb2, b, K, N, ldb, 64, kBK, bf16);
+    else if (tb && cfg.mc == 2) ok2 = make_map(tmb2, b, N, K, ldb, kBK, 64, bf16);
+    else std::memcpy(tmb2, tmb, sizeof(*tmb));
     p->a_mn = ta;
     p->b_kmajor = tb;
     p->b_3d = b3d ? 1 : 0;
@@ -528,8 +554,8 @@ struct Plan {
 // allow_split = false (callers without scratch for the partial sums) leaves
 // only the column-part tail.
 Plan choose_plan(const Cfg &cfg, int64_t M, int64_t N, int64_t K, int num_sms, bool allow_split = true) {
-    const int64_t groups = cfg.cg == 2 ? num_sms / 2 : num_sms;
-    const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn);
+    const int64_t groups = num_sms / cfg.ctas();
+    const int64_t tiles = cdiv(M, cfg.rows()) * cdiv(N, cfg.bn);
     const int64_t kb = cdiv(K, kBK);
     if (allow_split) {
         if (const char *f = std::getenv("TGEMM_SPLIT_K")) return {std::max(1, std::atoi(f)), 0, 0, 1};
@@ -554,7 +580,7 @@ Plan choose_plan(const Cfg &cfg, int64_t M, int64_t N, int64_t K, int num_sms, b
 int64_t partial_floats_per_unit(const Cfg &cfg) {
     const int cw = cfg.cw();
     const int64_t max_sub = ((cfg.bn / cw + 1) / 2) * cw / 32;
-    return static_cast<int64_t>(cfg.cg) * kEpiWarps * max_sub * 1024;
+    return static_cast<int64_t>(cfg.ctas()) * kEpiWarps * max_sub * 1024;
 }
 
 tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void *bias, void *C,
@@ -652,9 +678,9 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
             p.test_extra_tx = 16;
         }
     if (p.split_k > 1) {
-        const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn) - plan.split_first;
+        const int64_t tiles = cdiv(M, cfg.rows()) * cdiv(N, cfg.bn) - plan.split_first;
         const int64_t pbytes = tiles * p.split_k * partial_floats_per_unit(cfg) * 4;
-        const int64_t cbytes = tiles * cfg.cg * kEpiWarps * 4;
+        const int64_t cbytes = tiles * cfg.ctas() * kEpiWarps * 4;
         if (cudaMallocFromPoolAsync(&scratch_split, static_cast<size_t>(pbytes + cbytes), d->pool, stream) !=
                 cudaSuccess ||
             cudaMemsetAsync(static_cast<char *>(scratch_split) + pbytes, 0, static_cast<size_t>(cbytes), stream) !=
@@ -1134,7 +1160,7 @@ extern "C" tgemm_status tgemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
         return TGEMM_ERR_INVALID_ARG;
     const Cfg cfg = choose_config(M, N, K, num_sms);
     Plan plan = choose_plan(cfg, M, N, K, num_sms);
-    const int64_t tiles = cdiv(M, kBM * cfg.cg) * cdiv(N, cfg.bn);
+    const int64_t tiles = cdiv(M, cfg.rows()) * cdiv(N, cfg.bn);
     // The same normalisation as the launch.
     int split_k = std::max(1, plan.split_k);
     const int64_t kb = cdiv(K, kBK);
@@ -1147,8 +1173,8 @@ extern "C" tgemm_status tgemm_plan(int64_t M, int64_t N, int64_t K, int num_sms,
     if (parts == 1) narrow_first = split_first;
     const int64_t units = count_units(tiles, split_k, split_first, narrow_first, parts);
     if (tiles > INT32_MAX || units > INT32_MAX) return TGEMM_ERR_INVALID_ARG;
-    const int64_t groups = std::min<int64_t>(units, num_sms / cfg.cg);
-    const int64_t v[10] = {cfg.bn, cfg.cg, cfg.stages, tiles, groups, split_k, split_first, narrow_first, parts, units};
+    const int64_t groups = std::min<int64_t>(units, num_sms / cfg.ctas());
+    const int64_t v[10] = {cfg.bn, cfg.ctas(), cfg.stages, tiles, groups, split_k, split_first, narrow_first, parts, units};
     for (int i = 0; i < 10; ++i) out[i] = static_cast<int32_t>(v[i]);
     return TGEMM_OK;
 }

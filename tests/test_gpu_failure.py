@@ -20,10 +20,10 @@ pytestmark = pytest.mark.gpu
 TIMEOUT = 6   # TGEMM_ERR_TIMEOUT
 
 
-@pytest.mark.parametrize("cfg", ["256x2", "128"])
+@pytest.mark.parametrize("cfg", ["256x4", "256x2", "128"])
 def test_operand_wait_runs_out_and_context_stays_usable(cuda_lib, monkeypatch, cfg):
     monkeypatch.setenv("TGEMM_FORCE_CFG", cfg)
-    M, N, K = 256, 512, 512
+    M, N, K = 512, 512, 512
     assert cuda_lib.tgemm_last_device_status() == 0
     monkeypatch.setenv("TGEMM_TEST_STALL", "1")
     t0 = time.monotonic()

@@ -98,7 +98,7 @@ def test_small_and_odd_shapes(cuda_lib, M, N, K):
     assert_close(got, ref, dtype, f"{M}x{N}x{K} {epi} {dtype}", magnitude(inputs, N, K), K)
 
 
-CONFIGS = ["64", "128", "192", "256", "128x2", "224x2", "256x2"]
+CONFIGS = ["64", "128", "192", "256", "128x2", "224x2", "256x2", "256x4"]
 
 
 @pytest.mark.parametrize("bn", CONFIGS)
@@ -179,6 +179,7 @@ def test_decode_shapes_split_automatically(cuda_lib, M):
 # tiles are cut into column parts that run as narrower MMAs.
 NARROW_CASES = [
     ("256x2", 2048, 2560, 320, 2),     # 8 x 10 = 80 pair tiles: 4 cut in two
+    ("256x4", 2048, 2560, 320, 2),     # 4 x 10 = 40 shared-B tiles on 38 clusters: 2 cut in two
     ("256x2", 2048, 2404, 200, 2),     # last column block has 100 columns: one part lies past N
     ("256", 2560, 2048, 256, 4),       # 20 x 8 = 160 tiles on 152 SMs: 8 cut in four (64 columns)
     ("128", 2560, 1088, 130, 2),       # 20 x 9 = 180 tiles: 28 cut in two
@@ -211,6 +212,8 @@ def test_narrow_tail(cuda_lib, monkeypatch, cfg, M, N, K, parts):
 # finish adds the fp32 partials in range order before the epilogue.
 TAIL_SPLIT_CASES = [
     ("256x2", 2048, 2560, 4096, 4),    # 8 x 10 = 80 pair tiles: 4 left, 64 k-blocks in 4 ranges
+    ("256x4", 2048, 2560, 4096, 4),    # 4 x 10 = 40 shared-B tiles: 2 left, 64 k-blocks in 4 ranges
+    ("256x4", 2560, 2404, 2000, 2),    # 5 x 10 = 50 tiles: 12 left in 2 ranges, ragged k-block and columns
     ("224x2", 2048, 2240, 3072, 3),    # 80 tiles of 224 columns: 4 left, 48 k-blocks in 3 ranges
     ("256x2", 2048, 2404, 2000, 2),    # ragged k-block and a last column block of 100 columns
     ("256", 2560, 2048, 4096, 4),      # 160 single-CTA tiles: 8 left over
@@ -243,7 +246,7 @@ def test_k_split_tail(cuda_lib, monkeypatch, cfg, M, N, K, ranges):
     check_epilogue(whole[rows], inputs, M, N, K, "bf16", "bias_gelu", f"{cfg} whole tiles gelu", rows=rows)
 
 
-@pytest.mark.parametrize("cfg", ["256x2", "128x2", "256", "192", "128", "64"])
+@pytest.mark.parametrize("cfg", ["256x4", "256x2", "128x2", "256", "192", "128", "64"])
 @pytest.mark.parametrize("M,N,K,ldb", [(700, 1024, 300, None),     # N a multiple of 64: one 3-D box per k-block
                                        (700, 1000, 300, 1024),     # last chunk past N inside the pitch
                                        (700, 1000, 300, None)])    # ... outside it: 2-D copies
