@@ -42,30 +42,43 @@ def run(A: torch.Tensor, B: torch.Tensor, bias, C: torch.Tensor, epilogue="bias_
     (stride(0) >= width); bias is [N] or None.  Raises TgemmError on a status
     other than TGEMM_OK.
     """
-    _check_2d("A", A), _check_2d("B", B), _check_2d("C", C)
-    M, K = (A.shape[1], A.shape[0]) if transpose_a else tuple(A.shape)
-    K2, N = (B.shape[1], B.shape[0]) if transpose_b else tuple(B.shape)
-    if K2 != K or tuple(C.shape) != (M, N):
+    # Each tensor attribute read costs a trip into torch, so every one is read once.
+    sa, sb, sc = A.stride(), B.stride(), C.stride()
+    if len(sa) != 2 or len(sb) != 2 or len(sc) != 2 or sa[1] != 1 or sb[1] != 1 or sc[1] != 1:
+        for name, t in (("A", A), ("B", B), ("C", C)):
+            _check_2d(name, t)
+    (a0, a1), (b0, b1), (M, N) = A.shape, B.shape, C.shape
+    M2, K = (a1, a0) if transpose_a else (a0, a1)
+    K2, N2 = (b1, b0) if transpose_b else (b0, b1)
+    if K2 != K or M2 != M or N2 != N:
         raise ValueError(f"shape mismatch A{tuple(A.shape)} B{tuple(B.shape)} C{tuple(C.shape)}")
-    if not (A.dtype == B.dtype == C.dtype) or A.dtype not in _DT:
+    dt = A.dtype
+    code = _DT.get(dt)
+    if code is None or B.dtype != dt or C.dtype != dt:
         raise ValueError("A, B and C must share dtype float16 or bfloat16")
-    if bias is not None and (bias.dtype != A.dtype or bias.dim() != 1 or bias.numel() != N
-                             or bias.stride(0) != 1):
-        raise ValueError("bias must be a contiguous [N] tensor of the same dtype")
-    s = stream if stream is not None else torch.cuda.current_stream(A.device)
-    with torch.cuda.device(A.device):
-        if transpose_a or transpose_b:
-            st = tgemm_run_ex(A.data_ptr(), B.data_ptr(), bias.data_ptr() if bias is not None else 0,
-                              C.data_ptr(), M, N, K, A.stride(0), B.stride(0), C.stride(0),
-                              _DT[A.dtype], _epi(epilogue), int(transpose_a), int(transpose_b),
-                              s.cuda_stream)
-        else:
-            st = tgemm_run(A.data_ptr(), B.data_ptr(), bias.data_ptr() if bias is not None else 0,
-                           C.data_ptr(), M, N, K, A.stride(0), B.stride(0), C.stride(0), _DT[A.dtype],
-                           _epi(epilogue), s.cuda_stream)
+    bptr = 0
+    if bias is not None:
+        if bias.dtype != dt or bias.dim() != 1 or bias.numel() != N or bias.stride(0) != 1:
+            raise ValueError("bias must be a contiguous [N] tensor of the same dtype")
+        bptr = bias.data_ptr()
+    dev = A.device
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    args = (A.data_ptr(), B.data_ptr(), bptr, C.data_ptr(), M, N, K, sa[0], sb[0], sc[0], code, _epi(epilogue))
+    # The library works on the current device: switch only when A is elsewhere.
+    if dev.index == torch.cuda.current_device():
+        st = _call(args, transpose_a, transpose_b, s.cuda_stream)
+    else:
+        with torch.cuda.device(dev):
+            st = _call(args, transpose_a, transpose_b, s.cuda_stream)
     if st != 0:
         raise TgemmError(st)
     return C
+
+
+def _call(args, transpose_a, transpose_b, stream) -> int:
+    if transpose_a or transpose_b:
+        return tgemm_run_ex(*args, int(transpose_a), int(transpose_b), stream)
+    return tgemm_run(*args, stream)
 
 
 def run_host(A: torch.Tensor, B: torch.Tensor, bias, C: torch.Tensor, epilogue="bias_relu",

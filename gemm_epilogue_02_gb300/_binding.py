@@ -74,8 +74,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
 def tgemm_run(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
               ldc: int, dtype: int, epilogue: int, stream: int = 0) -> int:
     """Raw C-ABI call with device pointers (ints); returns the status code."""
-    return load().tgemm_run(A or None, B or None, bias or None, C or None, M, N, K, lda, ldb, ldc,
-                            dtype, epilogue, stream or None)
+    lib = _lib if _lib is not None else load()
+    return lib.tgemm_run(A or None, B or None, bias or None, C or None, M, N, K, lda, ldb, ldc,
+                         dtype, epilogue, stream or None)
 
 
 def tgemm_run_ex(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,

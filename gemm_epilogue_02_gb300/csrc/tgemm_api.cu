@@ -297,9 +297,7 @@ double effective_waves(const Cfg &cfg, int64_t tiles, int64_t groups) {
 // effective waves x width x a relative cost per column (narrow single-CTA tiles
 // re-read A from shared memory more often, and a 224-wide pair tile runs at
 // the speed of a 256-wide one; measured on the 8192^3 workload).  CTA pairs
-// are preferred whenever their tiles fill every SM pair at least once, and
-// clusters of two pairs sharing B whenever their 512 x 256 tiles fill every
-// cluster at least once (a quarter less operand traffic from L2 per SM).
+// are preferred whenever their tiles fill every SM pair at least once.
 Cfg choose_config(int64_t M, int64_t N, int64_t K, int num_sms) {
     if (const char *f = std::getenv("TGEMM_FORCE_CFG")) {
         const std::string v(f);
@@ -316,7 +314,12 @@ Cfg choose_config(int64_t M, int64_t N, int64_t K, int num_sms) {
     (void)K;
     const int pairs = num_sms / 2;
     if (M > kBM && cdiv(M, 2 * kBM) * cdiv(N, 256) >= pairs) {
-        const bool shared_b = M > 2 * kBM && cdiv(M, 4 * kBM) * cdiv(N, 256) >= num_sms / 4;
+        // Clusters of two pairs sharing B are built and tested but taken only on
+        // request (TGEMM_FORCE_CFG=256x4): their rings advance in lockstep (a
+        // stage is refilled once both pairs are done with it), and that coupling
+        // cost more than the quarter of L2 operand traffic it saves (same-process
+        // A/B on GB300: 4096^3 93.0 vs 88.3 us, 8192^3 bf16 611.6 vs 590.9 us).
+        const bool shared_b = false;
         const Cand cands[3] = {{kCfg256x4, 1.0}, {kCfg256x2, 1.0}, {kCfg224x2, 256.0 / 224.0}};
         Cfg best = kCfg256x2;
         double best_cost = 1e300;

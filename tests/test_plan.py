@@ -2,9 +2,8 @@
 through tgemm_plan: host logic only, so it runs without a GPU.
 
 The expected plans are worked out by hand from the rules the planner states:
-CTA pairs with 256 x 256 tiles whenever those tiles fill every SM pair once,
-and clusters of two such pairs sharing B (512 x 256 tiles on 4 CTAs)
-whenever those fill every cluster of 4 SMs once;
+CTA pairs with 256 x 256 tiles whenever those tiles fill every SM pair once
+(clusters of two pairs sharing B, 512 x 256 tiles on 4 CTAs, only on request);
 the tiles of a last partial wave cut in k into 2-4 ranges of at least 16
 k-blocks when those pieces fit one wave, else into column parts that still
 fit one wave; split-K of every tile only for problems with under half a wave
@@ -26,48 +25,39 @@ def _no_overrides(monkeypatch):
         monkeypatch.delenv(v, raising=False)
 
 
-def test_square_4096_shared_b_clusters_with_a_k_split_tail():
-    # 8 x 16 = 128 tiles of 512 x 256 on 38 clusters: 3 whole waves; the 14
-    # tiles left have their 64 k-blocks cut into 2 ranges (28 pieces <= 38; 3
-    # would not fit).
+def test_square_4096_pairs_with_a_k_split_tail():
+    # 16 x 16 = 256 tiles on 76 pairs: 3 whole waves; the 28 tiles left have
+    # their 64 k-blocks cut into 2 ranges (56 pieces <= 76; 3 would not fit).
+    p = tg.tgemm_plan(4096, 4096, 4096, SMS)
+    assert (p["bn"], p["cg"], p["tiles"], p["groups"]) == (256, 2, 256, 76)
+    assert (p["split_k"], p["split_first"], p["narrow_first"], p["narrow_parts"]) == (2, 228, 228, 1)
+    assert p["units"] == 2 * 28 + 228
+
+
+def test_square_4096_narrow_tail_on_request(monkeypatch):
+    # TGEMM_TAIL_SPLIT=1: the 28 tiles are cut into two column parts instead.
+    monkeypatch.setenv("TGEMM_TAIL_SPLIT", "1")
+    p = tg.tgemm_plan(4096, 4096, 4096, SMS)
+    assert (p["split_k"], p["narrow_first"], p["narrow_parts"]) == (1, 228, 2)
+    assert p["units"] == 228 + 2 * 28
+
+
+def test_square_4096_shared_b_clusters_on_request(monkeypatch):
+    # TGEMM_FORCE_CFG=256x4: 8 x 16 = 128 tiles of 512 x 256 on 38 clusters of
+    # 4 CTAs: 3 whole waves; the 14 tiles left have their 64 k-blocks cut into
+    # 2 ranges (28 pieces <= 38; 3 would not fit).
+    monkeypatch.setenv("TGEMM_FORCE_CFG", "256x4")
     p = tg.tgemm_plan(4096, 4096, 4096, SMS)
     assert (p["bn"], p["cg"], p["tiles"], p["groups"]) == (256, 4, 128, 38)
     assert (p["split_k"], p["split_first"], p["narrow_first"], p["narrow_parts"]) == (2, 114, 114, 1)
     assert p["units"] == 2 * 14 + 114
 
 
-def test_square_4096_narrow_tail_on_request(monkeypatch):
-    # TGEMM_TAIL_SPLIT=1: the 14 tiles are cut into two column parts instead.
-    monkeypatch.setenv("TGEMM_TAIL_SPLIT", "1")
-    p = tg.tgemm_plan(4096, 4096, 4096, SMS)
-    assert (p["split_k"], p["narrow_first"], p["narrow_parts"]) == (1, 114, 2)
-    assert p["units"] == 114 + 2 * 14
-
-
-def test_square_4096_pairs_on_request(monkeypatch):
-    # TGEMM_FORCE_CFG=256x2: 16 x 16 = 256 pair tiles on 76 pairs, 28 left in 2 ranges.
-    monkeypatch.setenv("TGEMM_FORCE_CFG", "256x2")
-    p = tg.tgemm_plan(4096, 4096, 4096, SMS)
-    assert (p["bn"], p["cg"], p["tiles"], p["groups"]) == (256, 2, 256, 76)
-    assert (p["split_k"], p["split_first"], p["units"]) == (2, 228, 2 * 28 + 228)
-
-
 def test_square_8192():
-    # 16 x 32 = 512 tiles: 13 waves of 38 and 18 tiles in two k ranges (36 <= 38).
+    # 32 x 32 = 1024 tiles: 13 waves of 76 and 36 tiles in two k ranges (72 <= 76).
     p = tg.tgemm_plan(8192, 8192, 8192, SMS)
-    assert (p["bn"], p["cg"], p["tiles"]) == (256, 4, 512)
-    assert (p["split_k"], p["split_first"], p["narrow_parts"], p["units"]) == (2, 494, 1, 36 + 494)
-
-
-def test_pairs_or_shared_b_clusters():
-    # 256 rows cannot hold two pairs: 1 x 76 = 76 pair tiles, plain pairs.
-    p = tg.tgemm_plan(256, 256 * 76, 4096, SMS)
-    assert (p["bn"], p["cg"], p["tiles"]) == (256, 2, 76)
-    # 768 rows: 3 x 26 = 78 pair tiles fill the 76 pairs, and 2 x 26 = 52
-    # shared-B tiles fill the 38 clusters (pair tiles filling 76 pairs always
-    # give shared-B tiles that fill 38 clusters when there are two pair rows).
-    p = tg.tgemm_plan(768, 256 * 26, 4096, SMS)
-    assert (p["bn"], p["cg"], p["tiles"], p["groups"]) == (256, 4, 52, 38)
+    assert (p["bn"], p["cg"], p["tiles"]) == (256, 2, 1024)
+    assert (p["split_k"], p["split_first"], p["narrow_parts"], p["units"]) == (2, 988, 1, 72 + 988)
 
 
 def test_tail_ranges_capped_by_k_and_four(monkeypatch):
@@ -91,16 +81,14 @@ def test_decode_shape_splits_k():
 
 
 def test_whole_waves_are_not_cut():
-    p = tg.tgemm_plan(256 * 4, 256 * 19, 512, SMS)   # 2 x 19 = 38 shared-B tiles: one whole wave
-    assert (p["bn"], p["cg"], p["tiles"], p["narrow_parts"], p["units"]) == (256, 4, 38, 1, 38)
-    p = tg.tgemm_plan(256 * 2, 256 * 38, 512, SMS)   # 2 x 38 = 76 pair tiles, 1 x 38 shared-B tiles
-    assert (p["bn"], p["cg"], p["tiles"], p["narrow_parts"], p["units"]) == (256, 4, 38, 1, 38)
+    p = tg.tgemm_plan(256 * 4, 256 * 19, 512, SMS)   # 4 x 19 = 76 pair tiles: one whole wave
+    assert (p["bn"], p["cg"], p["tiles"], p["narrow_parts"], p["units"]) == (256, 2, 76, 1, 76)
 
 
 def test_overrides(monkeypatch):
     monkeypatch.setenv("TGEMM_TAIL_SPLIT", "0")
     p = tg.tgemm_plan(4096, 4096, 4096, SMS)
-    assert (p["narrow_parts"], p["narrow_first"], p["units"]) == (1, 128, 128)
+    assert (p["narrow_parts"], p["narrow_first"], p["units"]) == (1, 256, 256)
     monkeypatch.delenv("TGEMM_TAIL_SPLIT")
     monkeypatch.setenv("TGEMM_FORCE_CFG", "256")
     p = tg.tgemm_plan(2560, 2048, 512, SMS)           # 20 x 8 = 160 tiles: 8 left over
