@@ -90,6 +90,9 @@ struct KParams {
     // per-stage byte count (stage_tx_narrow).  No reduction is needed: every
     // output element is still one whole k loop.
     int narrow_first, narrow_parts;
+    // 1: the split-K pieces of a k-split tail run after the whole tiles
+    // instead of before them.
+    int split_last;
     uint32_t stage_tx_narrow, idesc_narrow;
     float *partials;
     unsigned int *counters;
@@ -102,6 +105,9 @@ struct KParams {
     // which then never completes, so that the operand wait runs out and the
     // timeout path (status word, drain, TMEM release) is exercised.
     uint32_t test_extra_tx;
+    // k-blocks before the end of a unit at which the producer asks L2 for the
+    // first `STAGES` k-blocks of its next unit (0: no prefetch).
+    int l2_prefetch_ahead;
     uint32_t idesc;
     unsigned int *status;      // device status word
 #ifdef TGEMM_TRACE
@@ -238,7 +244,7 @@ struct Unit {
 };
 
 // Unit order: split-K pieces, then whole tiles 0 .. narrow_first-1, then the
-// column parts of the narrow tiles.
+// column parts of the narrow tiles (with split_last, the split-K pieces last).
 __device__ __forceinline__ Unit unit_info(int u, const KParams &p, int bn) {
     Unit w;
     w.kb0 = 0;
@@ -246,15 +252,17 @@ __device__ __forceinline__ Unit unit_info(int u, const KParams &p, int bn) {
     w.range = -1;
     w.col0 = 0;
     w.width = bn;
-    if (u < p.num_split_units) {
-        const int i = u / p.split_k;
+    const int first_split = p.split_last ? p.num_units - p.num_split_units : 0;
+    if (u >= first_split && u - first_split < p.num_split_units) {
+        const int s = u - first_split;
+        const int i = s / p.split_k;
         w.t = p.split_first + i;
-        w.range = u - i * p.split_k;
+        w.range = s - i * p.split_k;
         w.kb0 = w.range * p.kb_per_split;
         w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
         return w;
     }
-    const int v = u - p.num_split_units;
+    const int v = p.split_last ? u : u - p.num_split_units;
     if (v < p.narrow_first) {
         w.t = v;
         return w;
@@ -272,19 +280,35 @@ __device__ __forceinline__ float epi_relu(float v) {
     return (v <= 0.0f) ? 0.0f : v;
 }
 
+// 1 / y for 1 <= y <= 2^120 on the FMA pipe, leaving the special-function
+// unit to the exponential.  The seed reads y's bit pattern as a piecewise-linear
+// logarithm and negates it (the reciprocal trick of J. Blinn, "Floating-point
+// tricks", IEEE Computer Graphics and Applications 17(4), 1997), with the
+// constant chosen by a numerical search to minimise the seed's relative error
+// (5.1 %); two Newton-Raphson steps r <- r (2 - y r) each square that error,
+// leaving at most 6.6e-6 in fp32.
+__device__ __forceinline__ float rcp_newton(float y) {
+    float r = __int_as_float(0x7EF311C4 - __float_as_int(y));
+    r = r * fmaf(-y, r, 2.0f);
+    return r * fmaf(-y, r, 2.0f);
+}
+
 // The tanh-form GELU of "TileLang で GPU カーネル設計を解説" §4, written as a
 // sigmoid: x / (1 + exp(-1.5957691216 (x + 0.044715 x^3))).  The exponential
 // is taken base 2 with the constants folded, exp(-1.5957691216 (x + 0.044715
 // x^3)) = 2^(x (c1 + c2 x^2)), c1 = -1.5957691216 log2(e), c2 = 0.044715 c1,
 // so that each element costs three multiply-adds before the hardware 2^z
-// (`ex2.approx`) and the reciprocal; in fp32 the folded form stays within
-// about 2e-7 |x| of the exact function.  Large negative x gives 2^z -> inf
-// and x * 0 = -0; NaN propagates.
+// (`ex2.approx`, the one special-function operation per element) and the
+// reciprocal above; in fp32 the result stays within about 7e-6 |x| of the
+// exact function.  For z >= 120 (x below about -10.5) the quotient is below
+// 2^-120 |x| and is returned as x * 0 (-0 for finite x, NaN for -inf, as
+// x / inf gives); NaN propagates; +inf gives +inf.
 __device__ __forceinline__ float epi_gelu(float x) {
     const float z = x * fmaf(-0.10294324f, x * x, -2.3022082f);
     float e;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z));
-    return __fdividef(x, 1.0f + e);
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fminf(z, 120.0f)));
+    const float r = rcp_newton(1.0f + e);
+    return x * (z < 120.0f ? r : 0.0f);
 }
 
 template <bool kBf16>
@@ -457,9 +481,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b_sub = narrow ? (w.width / CG) / 64 : L::kBSub;
                 const uint32_t tx = narrow ? p.stage_tx_narrow : p.stage_tx;
                 const bool st_trace = (u == group_id + num_groups);
+                // The next unit's operands usually miss in L2 (a new tile), and every
+                // CTA switches tiles at about the same time: some k-blocks before
+                // the end of this unit, ask L2 for the next unit's first ring of
+                // k-blocks so that they are on chip when its loads go out.
+                const int pf_at = (p.l2_prefetch_ahead > 0 && u + num_groups < p.num_units)
+                                      ? max(w.kb0, w.kb1 - p.l2_prefetch_ahead) : -1;
+                auto prefetch_next = [&]() {
+                    const Unit nw = unit_info(u + num_groups, p, BN);
+                    int nm, nn;
+                    tile_coords(nw.t, p, nm, nn);
+                    const int na_row = nm * kUnitRows + cta_row0;
+                    const int nb_col = nn * BN + nw.col0 + static_cast<int>(rank) * (nw.width / CG);
+                    const bool nnarrow = nw.width != BN;
+                    for (int i = 0; i < STAGES && nw.kb0 + i < nw.kb1; ++i) {
+                        const int k0 = (nw.kb0 + i) * kBK;
+                        if (!p.a_mn) tma_prefetch_2d(&tmA, k0, na_row);
+                        else for (int j = 0; j < kBM / 64; ++j) tma_prefetch_2d(&tmA, na_row + j * 64, k0);
+                        if (p.b_kmajor) tma_prefetch_2d(&tmB, k0, nb_col);
+                        else if (p.b_3d && !nnarrow) tma_prefetch_3d(&tmB, 0, k0, nb_col >> 6);
+                        else for (int j = 0; j < (nnarrow ? (nw.width / CG) / 64 : L::kBSub); ++j)
+                            tma_prefetch_2d(p.b_3d ? &tmB2 : &tmB, nb_col + j * 64, k0);
+                    }
+                };
                 // A unit starts on a slot boundary; its last slot may hold fewer k-blocks.
                 for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
                     const int nkb = min(KSUB, w.kb1 - kb);
+                    if (kb <= pf_at && pf_at < kb + KSUB) prefetch_next();
                     const uint32_t fb = (CG == 1) ? full_bar(fbar) : leader_full(fbar);
                     auto load = [&](uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y) {
                         if constexpr (CG == 1) tma_load_2d(dst, m, fb, x, y);
