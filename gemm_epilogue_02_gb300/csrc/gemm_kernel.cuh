@@ -90,9 +90,6 @@ struct KParams {
     // per-stage byte count (stage_tx_narrow).  No reduction is needed: every
     // output element is still one whole k loop.
     int narrow_first, narrow_parts;
-    // 1: the split-K pieces of a k-split tail run after the whole tiles
-    // instead of before them.
-    int split_last;
     uint32_t stage_tx_narrow, idesc_narrow;
     float *partials;
     unsigned int *counters;
@@ -105,9 +102,6 @@ struct KParams {
     // which then never completes, so that the operand wait runs out and the
     // timeout path (status word, drain, TMEM release) is exercised.
     uint32_t test_extra_tx;
-    // k-blocks before the end of a unit at which the producer asks L2 for the
-    // first `STAGES` k-blocks of its next unit (0: no prefetch).
-    int l2_prefetch_ahead;
     uint32_t idesc;
     unsigned int *status;      // device status word
 #ifdef TGEMM_TRACE
@@ -244,7 +238,7 @@ struct Unit {
 };
 
 // Unit order: split-K pieces, then whole tiles 0 .. narrow_first-1, then the
-// column parts of the narrow tiles (with split_last, the split-K pieces last).
+// column parts of the narrow tiles.
 __device__ __forceinline__ Unit unit_info(int u, const KParams &p, int bn) {
     Unit w;
     w.kb0 = 0;
@@ -252,17 +246,15 @@ __device__ __forceinline__ Unit unit_info(int u, const KParams &p, int bn) {
     w.range = -1;
     w.col0 = 0;
     w.width = bn;
-    const int first_split = p.split_last ? p.num_units - p.num_split_units : 0;
-    if (u >= first_split && u - first_split < p.num_split_units) {
-        const int s = u - first_split;
-        const int i = s / p.split_k;
+    if (u < p.num_split_units) {
+        const int i = u / p.split_k;
         w.t = p.split_first + i;
-        w.range = s - i * p.split_k;
+        w.range = u - i * p.split_k;
         w.kb0 = w.range * p.kb_per_split;
         w.kb1 = min(p.num_kb, w.kb0 + p.kb_per_split);
         return w;
     }
-    const int v = p.split_last ? u : u - p.num_split_units;
+    const int v = u - p.num_split_units;
     if (v < p.narrow_first) {
         w.t = v;
         return w;
@@ -481,33 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b_sub = narrow ? (w.width / CG) / 64 : L::kBSub;
                 const uint32_t tx = narrow ? p.stage_tx_narrow : p.stage_tx;
                 const bool st_trace = (u == group_id + num_groups);
-                // The next unit's operands usually miss in L2 (a new tile), and every
-                // CTA switches tiles at about the same time: some k-blocks before
-                // the end of this unit, ask L2 for the next unit's first ring of
-                // k-blocks so that they are on chip when its loads go out.
-                const int pf_at = (p.l2_prefetch_ahead > 0 && u + num_groups < p.num_units)
-                                      ? max(w.kb0, w.kb1 - p.l2_prefetch_ahead) : -1;
-                auto prefetch_next = [&]() {
-                    const Unit nw = unit_info(u + num_groups, p, BN);
-                    int nm, nn;
-                    tile_coords(nw.t, p, nm, nn);
-                    const int na_row = nm * kUnitRows + cta_row0;
-                    const int nb_col = nn * BN + nw.col0 + static_cast<int>(rank) * (nw.width / CG);
-                    const bool nnarrow = nw.width != BN;
-                    for (int i = 0; i < STAGES && nw.kb0 + i < nw.kb1; ++i) {
-                        const int k0 = (nw.kb0 + i) * kBK;
-                        if (!p.a_mn) tma_prefetch_2d(&tmA, k0, na_row);
-                        else for (int j = 0; j < kBM / 64; ++j) tma_prefetch_2d(&tmA, na_row + j * 64, k0);
-                        if (p.b_kmajor) tma_prefetch_2d(&tmB, k0, nb_col);
-                        else if (p.b_3d && !nnarrow) tma_prefetch_3d(&tmB, 0, k0, nb_col >> 6);
-                        else for (int j = 0; j < (nnarrow ? (nw.width / CG) / 64 : L::kBSub); ++j)
-                            tma_prefetch_2d(p.b_3d ? &tmB2 : &tmB, nb_col + j * 64, k0);
-                    }
-                };
                 // A unit starts on a slot boundary; its last slot may hold fewer k-blocks.
                 for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
                     const int nkb = min(KSUB, w.kb1 - kb);
-                    if (kb <= pf_at && pf_at < kb + KSUB) prefetch_next();
                     const uint32_t fb = (CG == 1) ? full_bar(fbar) : leader_full(fbar);
                     auto load = [&](uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y) {
                         if constexpr (CG == 1) tma_load_2d(dst, m, fb, x, y);

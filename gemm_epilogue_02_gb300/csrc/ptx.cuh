@@ -148,21 +148,6 @@ __device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensor
         : "memory");
 }
 
-// L2 prefetch of a tiled box (no shared-memory destination, no completion).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *m, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int32_t x, int32_t y, int32_t z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // 3-D tiled loads (x innermost), for boxes that gather several 64-column
 // sub-tiles of one operand in a single copy.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, uint32_t bar,

@@ -416,13 +416,6 @@ int group_rows(const Cfg &cfg, int num_sms) {
     return std::max(1, g);
 }
 
-// k-blocks before the end of a unit at which the kernel prefetches the next
-// unit's first ring of operands into L2 (TGEMM_L2_PREFETCH overrides; 0 = off).
-int l2_prefetch_ahead() {
-    if (const char *e = std::getenv("TGEMM_L2_PREFETCH")) return std::max(0, std::atoi(e));
-    return 16;
-}
-
 // Work units of a plan: split-K pieces, whole tiles, narrow column parts.
 int64_t count_units(int64_t tiles, int split_k, int64_t split_first, int64_t narrow_first, int narrow_parts) {
     const int64_t split_units = (split_k > 1) ? (tiles - split_first) * split_k : 0;
@@ -452,7 +445,6 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
     p.num_tiles = static_cast<int>(tiles);
     p.num_split_units = static_cast<int>(split_units);
     p.num_units = static_cast<int>(units);
-    if (const char *e = std::getenv("TGEMM_SPLIT_LAST")) p.split_last = std::atoi(e) != 0 ? 1 : 0;
     int group_m = group_rows(cfg, d->num_sms);
     if (const char *g = std::getenv("TGEMM_GROUP_M")) group_m = std::max(1, std::atoi(g));
     p.group_m = std::min(p.num_m, group_m);
@@ -677,7 +669,6 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     p.split_first = static_cast<int>(plan.split_first);
     p.narrow_first = static_cast<int>(plan.narrow_first);
     p.narrow_parts = plan.narrow_parts;
-    p.l2_prefetch_ahead = l2_prefetch_ahead();
     if (const char *e = std::getenv("TGEMM_TEST_STALL"))
         if (std::atoi(e) != 0) {
             // Testing only (see KParams::test_extra_tx): every call with it set
@@ -830,7 +821,6 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
-    p.l2_prefetch_ahead = l2_prefetch_ahead();
     // No split-K here (its partials would need scratch); the narrow tail needs none.
     const Plan plan = choose_plan(cfg, M, N, K, d->num_sms, false);
     p.narrow_first = static_cast<int>(plan.narrow_first);

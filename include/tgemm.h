@@ -96,9 +96,10 @@ typedef enum {
  *
  * Environment overrides of the work plan, for testing and tuning only (results
  * change at most by the split-K note below): TGEMM_FORCE_CFG (tile shape:
- * 256, 192, 128, 64, 256x2, 224x2, 128x2), TGEMM_SPLIT_K (k ranges for every
- * tile), TGEMM_TAIL_SPLIT (the last partial wave's tiles: 0 = kept whole,
- * 1 = cut into column parts only), TGEMM_GROUP_M (row-blocks per
+ * 256, 192, 128, 64, 256x2, 224x2, 128x2, or 256x4: two 256 x 256 CTA pairs
+ * stacked in M that share B by cluster multicast), TGEMM_SPLIT_K (k ranges
+ * for every tile), TGEMM_TAIL_SPLIT (the last partial wave's tiles: 0 = kept
+ * whole, 1 = cut into column parts only), TGEMM_GROUP_M (row-blocks per
  * column sweep), TGEMM_NO_B3D (one copy per 64-column sub-tile of B).
  * TGEMM_TEST_STALL=1 (testing the failure path only) makes the GEMM kernel of
  * each call announce 16 bytes that never arrive for its first operand slot: its
@@ -260,7 +261,8 @@ tgemm_status tgemm_attention_fwd(const void *Q, const void *K, const void *V, vo
  * with split_k forced to 1.
  *
  * out (caller-owned, 10 int32 entries):
- *   [0] tile width BN (columns)      [1] CTAs per tile (1, or 2 for a pair: 256 rows)
+ *   [0] tile width BN (columns)      [1] CTAs per tile (1; 2 for a pair: 256 rows;
+ *                                        4 for two pairs sharing B: 512 rows)
  *   [2] shared-memory ring stages    [3] tiles = ceil(M / (128 * [1])) * ceil(N / BN)
  *   [4] persistent CTA groups launched (CTAs = [4] * [1])
  *   [5] split_k (1: no k split)      [6] first tile split in k (tiles from here on)
