@@ -131,9 +131,10 @@ struct KParams {
             p.trace[10240 + (kind) * 64 + (i)] = clock64();                                  \
     } while (0)
 // Epilogue timeline (SM clock cycles) of warp 2 of CTA 0 for its second unit:
-// p.trace[10688 + i], i = 0 accumulator ready, 1 bias handed over, 2 first
-// TMEM load landed, 3 + 2s sub-chunk s processed, 4 + 2s next load landed,
-// 20 done, 24 + s sub-chunk s's values packed, 28 + s its staging written.
+// p.trace[10688 + i], i = 0 accumulator ready, 21 first TMEM load issued, 22
+// bias strip stored, 1 next bias requested, 2 first TMEM load landed, 3 + 2s
+// sub-chunk s processed, 4 + 2s next load landed, 20 done, 24 + s sub-chunk
+// s's values packed, 28 + s its staging written.
 #define TGEMM_EPI_STAMP(i)                                                                   \
     do {                                                                                     \
         if (blockIdx.x == 0 && warp == 2 && lane == 0 && tile_i == 1 && (i) < 32)            \
@@ -272,35 +273,37 @@ __device__ __forceinline__ float epi_relu(float v) {
     return (v <= 0.0f) ? 0.0f : v;
 }
 
-// 1 / y for 1 <= y <= 2^120 on the FMA pipe, leaving the special-function
-// unit to the exponential.  The seed reads y's bit pattern as a piecewise-linear
-// logarithm and negates it (the reciprocal trick of J. Blinn, "Floating-point
-// tricks", IEEE Computer Graphics and Applications 17(4), 1997), with the
-// constant chosen by a numerical search to minimise the seed's relative error
-// (5.1 %); two Newton-Raphson steps r <- r (2 - y r) each square that error,
-// leaving at most 6.6e-6 in fp32.
-__device__ __forceinline__ float rcp_newton(float y) {
-    float r = __int_as_float(0x7EF311C4 - __float_as_int(y));
-    r = r * fmaf(-y, r, 2.0f);
-    return r * fmaf(-y, r, 2.0f);
-}
-
 // The tanh-form GELU of "TileLang で GPU カーネル設計を解説" §4, written as a
 // sigmoid: x / (1 + exp(-1.5957691216 (x + 0.044715 x^3))).  The exponential
 // is taken base 2 with the constants folded, exp(-1.5957691216 (x + 0.044715
 // x^3)) = 2^(x (c1 + c2 x^2)), c1 = -1.5957691216 log2(e), c2 = 0.044715 c1,
 // so that each element costs three multiply-adds before the hardware 2^z
-// (`ex2.approx`, the one special-function operation per element) and the
-// reciprocal above; in fp32 the result stays within about 7e-6 |x| of the
-// exact function.  For z >= 120 (x below about -10.5) the quotient is below
-// 2^-120 |x| and is returned as x * 0 (-0 for finite x, NaN for -inf, as
-// x / inf gives); NaN propagates; +inf gives +inf.
+// (`ex2.approx`) and the reciprocal; in fp32 the folded form stays within
+// about 2e-7 |x| of the exact function.  Large negative x gives 2^z -> inf
+// and x * 0 = -0; NaN propagates.  (A reciprocal on the FMA pipe, a bit-pattern
+// seed and two Newton steps, was measured slower: the epilogue is bound by
+// instruction issue, not by the special-function unit.)
 __device__ __forceinline__ float epi_gelu(float x) {
     const float z = x * fmaf(-0.10294324f, x * x, -2.3022082f);
     float e;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fminf(z, 120.0f)));
-    const float r = rcp_newton(1.0f + e);
-    return x * (z < 120.0f ? r : 0.0f);
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z));
+    return __fdividef(x, 1.0f + e);
+}
+
+// acc + bias for two columns whose 16-bit bias values are packed in `b`:
+// the mixed-precision add converts each 16-bit value to fp32 exactly and adds
+// with one rounding, the same result as a conversion followed by an fp32 add,
+// in one instruction.
+template <bool kBf16>
+__device__ __forceinline__ void add_bias2(uint32_t acc0, uint32_t acc1, uint32_t b, float &v0, float &v1) {
+    if constexpr (kBf16)
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %4;\n\t}"
+            : "=f"(v0), "=f"(v1) : "r"(b), "f"(__uint_as_float(acc0)), "f"(__uint_as_float(acc1)));
+    else
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %4;\n\t}"
+            : "=f"(v0), "=f"(v1) : "r"(b), "f"(__uint_as_float(acc0)), "f"(__uint_as_float(acc1)));
 }
 
 template <bool kBf16>
@@ -326,16 +329,8 @@ __device__ __forceinline__ void epi_math32(const uint32_t (&r)[32], const uint4 
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-            float b0, b1;
-            if constexpr (kBf16) {
-                b0 = __uint_as_float(w[h] << 16);            // bf16 -> fp32 is exact
-                b1 = __uint_as_float(w[h] & 0xFFFF0000u);
-            } else {
-                b0 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[h] & 0xFFFFu)));
-                b1 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[h] >> 16)));
-            }
-            float v0 = __uint_as_float(r[g * 8 + 2 * h]) + b0;
-            float v1 = __uint_as_float(r[g * 8 + 2 * h + 1]) + b1;
+            float v0, v1;
+            add_bias2<kBf16>(r[g * 8 + 2 * h], r[g * 8 + 2 * h + 1], w[h], v0, v1);
             if constexpr (kAct == 1) {
                 v0 = epi_relu(v0);
                 v1 = epi_relu(v1);
@@ -726,12 +721,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The unit's first TMEM load goes out before the bias hand-over,
             // which then hides its latency.
             if (n_sub > 0) tload(0, ra);
+            TGEMM_EPI_STAMP(21);
             // Publish this unit's bias strip, then start fetching the next unit's.
             __syncwarp();
 #pragma unroll
             for (int k = 0; k < kBiasPerLane; ++k)
                 if (lane + 32 * k < static_cast<int>(L::kBiasCols)) bias_s[lane + 32 * k] = bias_next[k];
             __syncwarp();
+            TGEMM_EPI_STAMP(22);
             if (has_next) fetch_bias(next_cb, next_wd);
             TGEMM_EPI_STAMP(1);
             uint32_t packed[CW / 2];
