@@ -54,7 +54,6 @@
 
 #include <type_traits>
 
-#include "bytes.cuh"
 #include "ptx.cuh"
 
 namespace tgemm {
@@ -783,44 +782,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_store_2d(&tmC, sb, n0, m0);
                         bulk_commit_group();
                     }
-                } else if (n0 + CW <= p.N) {
-                    // C's pitch is not a multiple of 16 bytes, so a row of the chunk
-                    // (2 * CW bytes) starts o bytes past a 16-byte boundary.  NCH lanes
-                    // per row: lane s > 0 stores the row's aligned 16-byte block s,
-                    // which holds the end of staged chunk s-1 and the start of chunk s;
-                    // lane 0 stores the partial blocks at both ends (o == 0: every
-                    // lane stores its chunk as it is).
-                    __syncwarp();
-                    constexpr int NCH = CW / 8;          // 16-byte chunks per staged row
-                    constexpr int RPS = 32 / NCH;        // rows per step
-                    const int s = lane % NCH;
-                    unsigned char *Cb = static_cast<unsigned char *>(p.C);
-#pragma unroll 2
-                    for (int r0 = 0; r0 < 32; r0 += RPS) {
-                        const int rr = r0 + lane / NCH;
-                        const int row = m0 + rr;
-                        if (row < p.M) {
-                            const long long off = (static_cast<long long>(row) * p.ldc + n0) * 2;
-                            const int o = static_cast<int>(off & 15);
-                            unsigned char *al = Cb + (off - o);
-                            const uint8_t *srow = sb_gen + rr * kRowBytes;
-                            auto chunk = [&](int j) {
-                                return *reinterpret_cast<const uint4 *>(srow + ((j ^ swz(rr)) << 4));
-                            };
-                            if (o == 0) {
-                                *reinterpret_cast<uint4 *>(al + 16 * s) = chunk(s);
-                            } else if (s > 0) {
-                                *reinterpret_cast<uint4 *>(al + 16 * s) = shift_bytes16(chunk(s - 1), chunk(s), 16 - o);
-                            } else {
-                                store_bytes16(al, chunk(0), o, 16, -o);
-                                store_bytes16(al + 16 * NCH, chunk(NCH - 1), 0, o, 16 - o);
-                            }
-                        }
-                    }
-                    __syncwarp();
                 } else {
                     __syncwarp();
                     // Masked, coalesced 2-byte stores: lane l writes columns 2l, 2l+1 of each row.
+                    // (16-byte stores shifted into each row's alignment were measured
+                    // slower on the unaligned-pitch workload, 306 against 286 us: the
+                    // rows' offsets differ, so the lanes of a warp diverge.)
                     unsigned short *Cg = reinterpret_cast<unsigned short *>(p.C);
                     const int col = n0 + 2 * lane;
                     if (lane < CW / 2) {
