@@ -403,17 +403,22 @@ cudaError_t launch_fused(DeviceInfo *d, unsigned bit, const CUtensorMap &ta, con
     return cudaLaunchKernelEx(&lc, kernel, ta, tb, tb2, tc, p);
 }
 
-// Row-blocks per column sweep of the tile order.  The tiles that run at the
-// same time (one per CTA group) then cover g row-blocks x groups / g column
-// blocks, whose operand panels, (g * 128 * cg + groups / g * bn) rows of K,
-// are what L2 must hold for each k step to be read once from DRAM; that sum
-// is smallest at g = sqrt(groups * bn / (128 * cg)).  Measured on 8192^3 bf16
-// (CTA pairs: g = 8): 970 MB of DRAM reads per launch against 1181 MB with
-// g = 16, at the same time.
-int group_rows(const Cfg &cfg, int num_sms) {
-    const double groups = static_cast<double>(num_sms / cfg.ctas());
-    const int g = static_cast<int>(std::lround(std::sqrt(groups * cfg.bn / cfg.rows())));
-    return std::max(1, g);
+// Row-blocks per column sweep of the tile order.  A group of g row-blocks is
+// swept column by column, so its A panel (g tiles' rows x K) is read from DRAM
+// once if L2 keeps it while the group's waves pass over B, and B is read once
+// per group: the fewer (taller) the groups, the less traffic, as long as the
+// panel fits.  g is the tallest panel within kL2PanelBytes, with the row-blocks
+// spread evenly over the groups.  Measured per launch (DRAM bytes read, ncu):
+// 8192^3 bf16 pairs, 4 MiB per row-block: g = 16 1181 MB, g = 8 970 MB; the
+// ragged 8191 x 6143 x 4104 case, 2 MiB per row-block: g = 16 198 MB, g = 9
+// 276 MB (four groups read B four times).
+constexpr int64_t kL2PanelBytes = 36ll << 20;
+int group_rows(const Cfg &cfg, int64_t M, int64_t K) {
+    const int64_t num_m = cdiv(M, cfg.rows());
+    const int64_t per_block = static_cast<int64_t>(cfg.rows()) * std::max<int64_t>(K, 1) * 2;
+    const int64_t g_max = std::max<int64_t>(1, kL2PanelBytes / per_block);
+    const int64_t groups = cdiv(num_m, g_max);
+    return static_cast<int>(std::max<int64_t>(1, cdiv(num_m, groups)));
 }
 
 // Work units of a plan: split-K pieces, whole tiles, narrow column parts.
@@ -445,7 +450,7 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
     p.num_tiles = static_cast<int>(tiles);
     p.num_split_units = static_cast<int>(split_units);
     p.num_units = static_cast<int>(units);
-    int group_m = group_rows(cfg, d->num_sms);
+    int group_m = group_rows(cfg, p.M, p.K);
     if (const char *g = std::getenv("TGEMM_GROUP_M")) group_m = std::max(1, std::atoi(g));
     p.group_m = std::min(p.num_m, group_m);
     p.idesc = idesc_f16(bf16, static_cast<uint32_t>(kBM * cfg.cg), static_cast<uint32_t>(cfg.bn),
