@@ -45,15 +45,20 @@ def metric_for(w):
     return METRIC_GELU if "gelu" in w.epilogue else METRIC
 DEFAULT_WORKLOAD = "c2"
 FLUSH_BYTES = 256 << 20            # > 2x the 129 MB L2
-KERNEL_SOURCES = ["gemm_epilogue_02_gb300/csrc/gemm_kernel.cuh", "gemm_epilogue_02_gb300/csrc/ptx.cuh",
-                  "gemm_epilogue_02_gb300/csrc/attn_kernel.cuh", "gemm_epilogue_02_gb300/csrc/aux_kernels.cuh",
-                  "gemm_epilogue_02_gb300/csrc/tgemm_api.cu"]
+# Sources that decide the device code of each kernel family (the host file
+# holds both families' launch code); a recorded DRAM traffic figure stands only
+# while these are unchanged.
+_CSRC = "gemm_epilogue_02_gb300/csrc/"
+KERNEL_SOURCES = {
+    "gemm": [_CSRC + f for f in ("gemm_kernel.cuh", "ptx.cuh", "aux_kernels.cuh", "bytes.cuh", "tgemm_api.cu")],
+    "attention": [_CSRC + f for f in ("attn_kernel.cuh", "gemm_kernel.cuh", "ptx.cuh", "tgemm_api.cu")],
+}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
-def kernel_hash() -> str:
+def kernel_hash(family: str = "gemm") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -78,7 +83,8 @@ def recorded_traffic(workload: str):
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("kernel_hash") == kernel_hash():
+        family = "attention" if workload in si.ATTN_WORKLOADS else "gemm"
+        if e and e.get("kernel_hash") == kernel_hash(family):
             return float(e["dram_bytes_per_launch"])
     except (OSError, ValueError):
         pass
