@@ -600,6 +600,7 @@ def run_tgemm_bench(args, world, rank, local):
     extras = {}
     if not args.no_extras and args.config == DEFAULT_WORKLOAD:
         extras["skinny"] = sub_record("c3", args, dev, stream, flush, world, local, check=not args.no_check)
+        extras["decode"] = sub_record("d16", args, dev, stream, flush, world, local, check=not args.no_check)
         extras["launch_bound"] = launch_bound_record("c0", args, dev, stream)
 
     status = tg.tgemm_last_device_status()
@@ -716,7 +717,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", action="store_true", help="skip the oracle check of the timed output")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the skinny and launch-bound sub-records of the default line")
+                    help="skip the skinny, decode and launch-bound sub-records of the default line")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--soak", type=float, default=1.0, help="minimum seconds of warm-up steps")
     ap.add_argument("--ref-rows", type=int, default=64, help="attention oracle query rows per reference step")

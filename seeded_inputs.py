@@ -47,8 +47,9 @@ class Workload:
         return 2 * self.M * self.N * self.K
 
 
-# The five workloads of the method's evaluation, plus the integer-exact variant
-# and the padded-pitch twin of the ragged case.
+# The five workloads of the method's evaluation, plus the integer-exact variant,
+# the padded-pitch twin of the ragged case, the GELU page's workload and a
+# decode shape.
 WORKLOADS = {
     "c0": Workload("gemm_relu_256_fp16", 256, 256, 256, "fp16", "relu", 0),
     "c1": Workload("gemm_bias_relu_4096_fp16", 4096, 4096, 4096, "fp16", "bias_relu", 1),
@@ -60,6 +61,8 @@ WORKLOADS = {
                     "bias_relu", 4, ldb=6144, ldc=6144),
     "c5": Workload("gemm_bias_gelu_4096x4096x1024_fp16", 4096, 4096, 1024, "fp16", "bias_gelu", 5,
                    kind="gelu"),
+    # A decode shape (few rows, long k): the small-M case split in k.
+    "d16": Workload("gemm_bias_relu_decode_16x4096x8192_fp16", 16, 4096, 8192, "fp16", "bias_relu", 6),
 }
 
 

@@ -41,7 +41,7 @@ def _lib(cuda_lib):
 
 
 # ------------------------------------------------------------------ workloads
-@pytest.mark.parametrize("name", ["c0", "c1", "c2", "c3", "c4", "c4p", "c5"])
+@pytest.mark.parametrize("name", ["c0", "c1", "c2", "c3", "c4", "c4p", "c5", "d16"])
 def test_workload_full_size(cuda_lib, name):
     w = si.WORKLOADS[name]
     inputs, got = run_tgemm(cuda_lib, w.M, w.N, w.K, w.dtype, w.epilogue, w.seed, w.kind,
