@@ -81,8 +81,8 @@ struct KParams {
     // those (tile, range) pieces and come first; the remaining units are whole
     // tiles 0 .. split_first-1.  Every epilogue warp of a piece writes its fp32
     // partial region to `partials`, and the last of the split_k warps covering
-    // that region (counted in `counters`, zero on entry, reset on exit) sums the
-    // partials in range order and runs the epilogue on the complete sum.
+    // that region (counted in `counters`) sums the partials in range order and
+    // runs the epilogue on the complete sum.
     int split_k, kb_per_split, split_first, num_split_units, num_units;
     // Narrow tail: tiles narrow_first .. split_first-1 (the last, partial wave)
     // are each cut into narrow_parts column parts of BN / narrow_parts columns;
@@ -92,7 +92,12 @@ struct KParams {
     int narrow_first, narrow_parts;
     uint32_t stage_tx_narrow, idesc_narrow;
     float *partials;
-    unsigned int *counters;
+    // Arrival counters, one 64-bit word per (split tile, CTA, epilogue warp):
+    // bits 16.. hold the launch that last counted there (`epoch`, unique per
+    // launch and stream), bits 0..15 its arrivals; a word left by another
+    // launch counts as zero, so the words never need clearing.
+    unsigned long long *counters;
+    unsigned long long epoch;
     int a_mn;                  // A stored transposed ([K, M], M contiguous): MN-major operand
     int b_kmajor;              // B stored transposed ([N, K], K contiguous): K-major operand
     int b_3d;                  // B [K, N] through a 3-D map (tmB): all BN/CG columns of a k-block in
@@ -852,7 +857,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(41);
                     unsigned int arrived = 0;
-                    if (lane == 0) arrived = atomicAdd(p.counters + ts * (kCluster * kEpiWarps) + wid, 1u);
+                    if (lane == 0) {
+                        // Count this arrival under this launch's epoch (a word still
+                        // holding another launch's epoch starts again from zero).
+                        unsigned long long *ctr = p.counters + ts * (kCluster * kEpiWarps) + wid;
+                        unsigned long long seen = *reinterpret_cast<volatile unsigned long long *>(ctr);
+                        for (;;) {
+                            const unsigned long long base = ((seen >> 16) == p.epoch) ? seen : (p.epoch << 16);
+                            const unsigned long long prev = atomicCAS(ctr, seen, base + 1ull);
+                            if (prev == seen) {
+                                arrived = static_cast<unsigned int>(base & 0xFFFFull);
+                                break;
+                            }
+                            seen = prev;   // another piece counted first: retry on its value
+                        }
+                    }
                     arrived = __shfl_sync(0xffffffffu, arrived, 0);
 #ifdef TGEMM_TRACE
                     if (warp == 2 && lane == 0 && tile_i == 0 && blockIdx.x < 160) {
@@ -910,7 +929,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp();
                         if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(44);
-                        if (lane == 0) p.counters[ts * (kCluster * kEpiWarps) + wid] = 0u;   // ready for the next launch
                     }
                 }
             } else if (n_sub == 0) {

@@ -15,6 +15,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 
 #include "../../include/tgemm.h"
 #include "aux_kernels.cuh"
@@ -29,6 +30,13 @@ constexpr int kVersion = 0x000100;
 
 __device__ unsigned int g_device_status;
 
+// Split-K arrival counters of one stream: kept between calls (never
+// cleared: each word carries the epoch of the launch that counted in it).
+struct CounterBuf {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+
 struct DeviceInfo {
     std::once_flag once;
     bool ok = false;        // CC 10.3
@@ -41,6 +49,8 @@ struct DeviceInfo {
     int max_clusters[32] = {};         // co-resident clusters per CTA-pair kernel (by attribute bit)
     cudaStream_t copy_in = nullptr;    // tgemm_run_host: host->device copies
     cudaStream_t copy_out = nullptr;   // tgemm_run_host: device->host copies
+    std::unordered_map<cudaStream_t, CounterBuf> counters;   // per stream, guarded by mu
+    unsigned long long epoch = 0;                            // last launch epoch, guarded by mu
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -688,17 +698,36 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     if (p.split_k > 1) {
         const int64_t tiles = cdiv(M, cfg.rows()) * cdiv(N, cfg.bn) - plan.split_first;
         const int64_t pbytes = tiles * p.split_k * partial_floats_per_unit(cfg) * 4;
-        const int64_t cbytes = tiles * cfg.ctas() * kEpiWarps * 4;
-        if (cudaMallocFromPoolAsync(&scratch_split, static_cast<size_t>(pbytes + cbytes), d->pool, stream) !=
-                cudaSuccess ||
-            cudaMemsetAsync(static_cast<char *>(scratch_split) + pbytes, 0, static_cast<size_t>(cbytes), stream) !=
-                cudaSuccess) {
+        const size_t cbytes = static_cast<size_t>(tiles * cfg.ctas() * kEpiWarps) * sizeof(unsigned long long);
+        if (cudaMallocFromPoolAsync(&scratch_split, static_cast<size_t>(pbytes), d->pool, stream) != cudaSuccess) {
             cudaGetLastError();
             release();
             return TGEMM_ERR_CUDA;
         }
         p.partials = static_cast<float *>(scratch_split);
-        p.counters = reinterpret_cast<unsigned int *>(static_cast<char *>(scratch_split) + pbytes);
+        // The stream's arrival counters: zeroed once when (re)allocated, then
+        // told apart between launches by the epoch (no clearing per call).
+        {
+            std::lock_guard<std::mutex> g(d->mu);
+            CounterBuf &cb = d->counters[stream];
+            if (cb.bytes < cbytes) {
+                void *fresh = nullptr;
+                const size_t want = std::max<size_t>(cbytes, 4096);
+                if (cudaMallocFromPoolAsync(&fresh, want, d->pool, stream) != cudaSuccess ||
+                    cudaMemsetAsync(fresh, 0, want, stream) != cudaSuccess) {
+                    cudaGetLastError();
+                    release();
+                    return TGEMM_ERR_CUDA;
+                }
+                if (cb.ptr) cudaFreeAsync(cb.ptr, stream);   // after the launches that used it
+                cb.ptr = fresh;
+                cb.bytes = want;
+            }
+            p.counters = static_cast<unsigned long long *>(cb.ptr);
+            d->epoch = (d->epoch + 1) & ((1ull << 48) - 1);
+            if (d->epoch == 0) d->epoch = 1;
+            p.epoch = d->epoch;
+        }
     }
     const cudaError_t e = launch_config(d, cfg, tma, tmb, tmb2, tmc, p, stream, bf16);
     release();
