@@ -92,10 +92,14 @@ struct KParams {
     int narrow_first, narrow_parts;
     uint32_t stage_tx_narrow, idesc_narrow;
     float *partials;
-    // Arrival counters, one 64-bit word per (split tile, CTA, epilogue warp):
-    // bits 16.. hold the launch that last counted there (`epoch`, unique per
-    // launch and stream), bits 0..15 its arrivals; a word left by another
-    // launch counts as zero, so the words never need clearing.
+    // Arrival counters, one 64-bit word per (split tile, CTA, epilogue warp).
+    // epoch != 0: bits 16.. hold the launch that last counted there (`epoch`,
+    // unique per launch), bits 0..15 its arrivals; a word left by another
+    // launch counts as zero, so the words never need clearing (one more L2
+    // round trip per arrival: used where the split pieces overlap whole
+    // tiles).  epoch == 0: the words are zero on entry (cleared on the stream
+    // before the launch) and plainly counted (the few-tile plans, whose
+    // reduction ends the launch).
     unsigned long long *counters;
     unsigned long long epoch;
     int a_mn;                  // A stored transposed ([K, M], M contiguous): MN-major operand
@@ -857,7 +861,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(41);
                     unsigned int arrived = 0;
-                    if (lane == 0) {
+                    if (lane == 0 && p.epoch == 0) {
+                        arrived = static_cast<unsigned int>(atomicAdd(p.counters + ts * (kCluster * kEpiWarps) + wid, 1ull));
+                    } else if (lane == 0) {
                         // Count this arrival under this launch's epoch (a word still
                         // holding another launch's epoch starts again from zero).
                         unsigned long long *ctr = p.counters + ts * (kCluster * kEpiWarps) + wid;

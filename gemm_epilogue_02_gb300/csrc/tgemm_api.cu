@@ -724,9 +724,22 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
                 cb.bytes = want;
             }
             p.counters = static_cast<unsigned long long *>(cb.ptr);
-            d->epoch = (d->epoch + 1) & ((1ull << 48) - 1);
-            if (d->epoch == 0) d->epoch = 1;
-            p.epoch = d->epoch;
+            if (plan.split_first > 0) {
+                // A k-split tail: its reductions overlap whole tiles, so an extra
+                // round trip per arrival is hidden and the clearing is not.
+                d->epoch = (d->epoch + 1) & ((1ull << 48) - 1);
+                if (d->epoch == 0) d->epoch = 1;
+                p.epoch = d->epoch;
+            } else {
+                // Every tile split (few tiles): the reduction ends the launch, so
+                // the counters are cleared on the stream and counted plainly.
+                p.epoch = 0;
+                if (cudaMemsetAsync(cb.ptr, 0, cbytes, stream) != cudaSuccess) {
+                    cudaGetLastError();
+                    release();
+                    return TGEMM_ERR_CUDA;
+                }
+            }
         }
     }
     const cudaError_t e = launch_config(d, cfg, tma, tmb, tmb2, tmc, p, stream, bf16);

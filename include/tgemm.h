@@ -113,7 +113,11 @@ typedef enum {
  * shapes) split the k loop of each tile across CTAs: fp32 partial sums go to
  * pool scratch and the last CTA to finish a tile region adds them in a fixed
  * order before the epilogue, so results are deterministic; they may differ
- * in the last bits from an unsplit run (different summation order).  Larger
+ * in the last bits from an unsplit run (different summation order).  The
+ * arrival counters of those regions live in a small buffer the library keeps
+ * for each stream it has launched such work on (8 bytes per region, at least
+ * 4 KiB, drawn from its pool and kept until the process exits); calls on one
+ * stream are ordered, so they share it safely.  Larger
  * problems whose tiles leave a last, partial wave cut those tiles the same
  * way (2-4 k ranges, each at least 16 k-blocks, when the pieces fit one wave;
  * same determinism, and those tiles may differ in the last bits from an
