@@ -176,6 +176,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Launched as a programmatic dependent of the stream's previous kernel: the
+    // set-up above overlapped its end; nothing in global memory is touched
+    // before it has completed.  The next kernel may launch from here on.
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer

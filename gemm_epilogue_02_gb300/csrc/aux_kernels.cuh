@@ -5,6 +5,7 @@
 #include <cstdint>
 
 #include "bytes.cuh"
+#include "ptx.cuh"
 
 namespace tgemm {
 
@@ -37,6 +38,9 @@ __device__ __forceinline__ uint4 load_block16(const unsigned char *__restrict__ 
 __global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t *__restrict__ src, long long lds,
                                                           uint16_t *__restrict__ dst, long long ldd,
                                                           long long rows, long long cols) {
+    // The fused kernel that reads dst may launch (and set itself up) now; it
+    // waits for this grid's completion before its first global access.
+    if (threadIdx.x == 0) griddep_launch_dependents();
     const long long vec_per_row = (cols + 7) / 8;
     const unsigned char *base = reinterpret_cast<const unsigned char *>(src);
     const long long span = ((rows - 1) * lds + cols) * 2;   // bytes of src the matrix covers

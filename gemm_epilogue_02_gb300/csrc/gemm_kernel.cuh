@@ -92,14 +92,13 @@ struct KParams {
     int narrow_first, narrow_parts;
     uint32_t stage_tx_narrow, idesc_narrow;
     float *partials;
-    // Arrival counters, one 64-bit word per (split tile, CTA, epilogue warp).
-    // epoch != 0: bits 16.. hold the launch that last counted there (`epoch`,
-    // unique per launch), bits 0..15 its arrivals; a word left by another
-    // launch counts as zero, so the words never need clearing (one more L2
-    // round trip per arrival: used where the split pieces overlap whole
-    // tiles).  epoch == 0: the words are zero on entry (cleared on the stream
-    // before the launch) and plainly counted (the few-tile plans, whose
-    // reduction ends the launch).
+    // Arrival counters, one 64-bit word per (split tile, CTA, epilogue warp):
+    // bits 16.. hold the launch that last counted there (`epoch`, unique per
+    // launch and increasing), bits 0..15 its arrivals.  Each piece's warp
+    // raises its word to at least epoch << 16 (an atomic maximum, sent when
+    // the unit starts, long before it is needed) and arrives with an atomic
+    // add, so a word left by an earlier launch counts from zero again and the
+    // words never need clearing.
     unsigned long long *counters;
     unsigned long long epoch;
     int a_mn;                  // A stored transposed ([K, M], M contiguous): MN-major operand
@@ -454,6 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Launched as a programmatic dependent of the stream's previous kernel: the
+    // set-up above overlapped its end; nothing in global memory is touched
+    // before it has completed.  The next kernel may launch from here on.
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
     if (threadIdx.x == 0) TGEMM_STAMP(1);
 
     if (warp == 0) {
@@ -704,6 +708,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool has_next = u + num_groups < p.num_units;
             int next_cb = 0, next_wd = 0;
             if (has_next) unit_cols(u + num_groups, next_cb, next_wd);
+            if (split >= 0 && lane == 0)
+                atomicMax(p.counters + (t - p.split_first) * (kCluster * kEpiWarps) + static_cast<int>(crank) * kEpiWarps + ew,
+                          p.epoch << 16);
             int ok = 1;
             if (lane == 0) ok = wait_bar<true>(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -861,23 +868,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(41);
                     unsigned int arrived = 0;
-                    if (lane == 0 && p.epoch == 0) {
-                        arrived = static_cast<unsigned int>(atomicAdd(p.counters + ts * (kCluster * kEpiWarps) + wid, 1ull));
-                    } else if (lane == 0) {
-                        // Count this arrival under this launch's epoch (a word still
-                        // holding another launch's epoch starts again from zero).
-                        unsigned long long *ctr = p.counters + ts * (kCluster * kEpiWarps) + wid;
-                        unsigned long long seen = *reinterpret_cast<volatile unsigned long long *>(ctr);
-                        for (;;) {
-                            const unsigned long long base = ((seen >> 16) == p.epoch) ? seen : (p.epoch << 16);
-                            const unsigned long long prev = atomicCAS(ctr, seen, base + 1ull);
-                            if (prev == seen) {
-                                arrived = static_cast<unsigned int>(base & 0xFFFFull);
-                                break;
-                            }
-                            seen = prev;   // another piece counted first: retry on its value
-                        }
-                    }
+                    if (lane == 0)   // the word is at least epoch << 16 already (raised at the unit's start)
+                        arrived = static_cast<unsigned int>(
+                            atomicAdd(p.counters + ts * (kCluster * kEpiWarps) + wid, 1ull) - (p.epoch << 16));
                     arrived = __shfl_sync(0xffffffffu, arrived, 0);
 #ifdef TGEMM_TRACE
                     if (warp == 2 && lane == 0 && tile_i == 0 && blockIdx.x < 160) {

@@ -393,23 +393,23 @@ cudaError_t launch_fused(DeviceInfo *d, unsigned bit, const CUtensorMap &ta, con
     if (const char *g = std::getenv("TGEMM_TRACE_MAX_GROUPS")) max_groups = std::max(1, std::min(max_groups, std::atoi(g)));
 #endif
     const int groups = static_cast<int>(std::min<int64_t>(tiles, max_groups));
-    if (kCl == 1) {
-        kernel<<<groups, kThreads, L::kDynamicBytes, s>>>(ta, tb, tb2, tc, p);
-        return cudaGetLastError();
-    }
+    // A programmatic dependent of the stream's previous kernel (the kernel waits
+    // for it before touching global memory), in clusters of kCl CTAs.
     cudaLaunchConfig_t lc;
     std::memset(&lc, 0, sizeof(lc));
-    cudaLaunchAttribute la[1];
-    la[0].id = cudaLaunchAttributeClusterDimension;
-    la[0].val.clusterDim.x = kCl;
-    la[0].val.clusterDim.y = 1;
-    la[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute la[2];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    la[1].id = cudaLaunchAttributeClusterDimension;
+    la[1].val.clusterDim.x = kCl;
+    la[1].val.clusterDim.y = 1;
+    la[1].val.clusterDim.z = 1;
     lc.gridDim = dim3(kCl * groups);
     lc.blockDim = dim3(kThreads);
     lc.dynamicSmemBytes = L::kDynamicBytes;
     lc.stream = s;
     lc.attrs = la;
-    lc.numAttrs = 1;
+    lc.numAttrs = (kCl > 1) ? 2 : 1;
     return cudaLaunchKernelEx(&lc, kernel, ta, tb, tb2, tc, p);
 }
 
@@ -706,9 +706,17 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
         }
         p.partials = static_cast<float *>(scratch_split);
         // The stream's arrival counters: zeroed once when (re)allocated, then
-        // told apart between launches by the epoch (no clearing per call).
+        // told apart between launches by the epoch (no clearing per call, so
+        // nothing is enqueued between the previous kernel and this one).
         {
             std::lock_guard<std::mutex> g(d->mu);
+            d->epoch = (d->epoch + 1) & ((1ull << 48) - 1);
+            if (d->epoch == 0) {
+                // Words may hold any earlier epoch (an atomic maximum would keep
+                // them): every stream's counters are renewed.
+                d->epoch = 1;
+                for (auto &kv : d->counters) kv.second.bytes = 0;
+            }
             CounterBuf &cb = d->counters[stream];
             if (cb.bytes < cbytes) {
                 void *fresh = nullptr;
@@ -724,22 +732,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
                 cb.bytes = want;
             }
             p.counters = static_cast<unsigned long long *>(cb.ptr);
-            if (plan.split_first > 0) {
-                // A k-split tail: its reductions overlap whole tiles, so an extra
-                // round trip per arrival is hidden and the clearing is not.
-                d->epoch = (d->epoch + 1) & ((1ull << 48) - 1);
-                if (d->epoch == 0) d->epoch = 1;
-                p.epoch = d->epoch;
-            } else {
-                // Every tile split (few tiles): the reduction ends the launch, so
-                // the counters are cleared on the stream and counted plainly.
-                p.epoch = 0;
-                if (cudaMemsetAsync(cb.ptr, 0, cbytes, stream) != cudaSuccess) {
-                    cudaGetLastError();
-                    release();
-                    return TGEMM_ERR_CUDA;
-                }
-            }
+            p.epoch = d->epoch;
         }
     }
     const cudaError_t e = launch_config(d, cfg, tma, tmb, tmb2, tmc, p, stream, bf16);
@@ -962,10 +955,21 @@ cudaError_t launch_attention(DeviceInfo *d, unsigned bit, const CUtensorMap &tq,
             d->attn_attr_set |= bit;
         }
     }
-    const dim3 grid(static_cast<unsigned>(p.H), static_cast<unsigned>(p.B),
-                    static_cast<unsigned>(cdiv(p.S, kAttnBM)));
-    kernel<<<grid, kAttnThreads, AttnSmem::kBytes, s>>>(tq, tk, tv, p);
-    return cudaGetLastError();
+    // A programmatic dependent of the stream's previous kernel (the kernel waits
+    // for it before touching global memory).
+    cudaLaunchConfig_t lc;
+    std::memset(&lc, 0, sizeof(lc));
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.gridDim = dim3(static_cast<unsigned>(p.H), static_cast<unsigned>(p.B),
+                      static_cast<unsigned>(cdiv(p.S, kAttnBM)));
+    lc.blockDim = dim3(kAttnThreads);
+    lc.dynamicSmemBytes = AttnSmem::kBytes;
+    lc.stream = s;
+    lc.attrs = la;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kernel, tq, tk, tv, p);
 }
 
 }  // namespace

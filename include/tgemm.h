@@ -117,7 +117,10 @@ typedef enum {
  * arrival counters of those regions live in a small buffer the library keeps
  * for each stream it has launched such work on (8 bytes per region, at least
  * 4 KiB, drawn from its pool and kept until the process exits); calls on one
- * stream are ordered, so they share it safely.  Larger
+ * stream are ordered, so they share it safely.  Kernels are enqueued as
+ * programmatic dependent launches: their set-up may overlap the end of the
+ * stream's previous kernel, but they touch no global memory before that
+ * kernel has completed, so stream order holds as for any launch.  Larger
  * problems whose tiles leave a last, partial wave cut those tiles the same
  * way (2-4 k ranges, each at least 16 k-blocks, when the pieces fit one wave;
  * same determinism, and those tiles may differ in the last bits from an
