@@ -454,8 +454,13 @@ def timed_steps(step, flush, args, dev, stream, world, local):
     steps bracketed by barriers, each launch timed with CUDA events on `stream`
     and L2 flushed before it.  Returns (launch ms list, wall seconds, clocks)."""
     with torch.cuda.stream(stream), ClockSampler(local) as clk:
+        # The first step carries one-time costs (kernel loading, the flush's
+        # first reduction): the soak's clock starts once it has finished.
+        flush()
+        step()
+        torch.cuda.synchronize(dev)
         t_soak = time.perf_counter()
-        done = 0
+        done = 1
         while done < args.warmup or time.perf_counter() - t_soak < args.soak:
             flush()
             step()
