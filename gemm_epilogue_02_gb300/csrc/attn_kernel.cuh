@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     // set-up above overlapped its end; nothing in global memory is touched
     // before it has completed.  The next kernel may launch from here on.
     griddep_wait();
-    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer

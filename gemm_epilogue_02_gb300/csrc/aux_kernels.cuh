@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t *__rest
                                                           long long rows, long long cols) {
     // The fused kernel that reads dst may launch (and set itself up) now; it
     // waits for this grid's completion before its first global access.
-    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_launch_dependents();
     const long long vec_per_row = (cols + 7) / 8;
     const unsigned char *base = reinterpret_cast<const unsigned char *>(src);
     const long long span = ((rows - 1) * lds + cols) * 2;   // bytes of src the matrix covers

@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // set-up above overlapped its end; nothing in global memory is touched
     // before it has completed.  The next kernel may launch from here on.
     griddep_wait();
-    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_launch_dependents();
     if (threadIdx.x == 0) TGEMM_STAMP(1);
 
     if (warp == 0) {
