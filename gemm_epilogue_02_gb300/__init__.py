@@ -11,9 +11,9 @@ import torch
 from ._binding import (  # noqa: F401
     TGEMM_BF16, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_GELU, TGEMM_EPI_BIAS_RELU, TGEMM_EPI_GELU,
     TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_F16,
-    EXPORTED, NOALLOC_SCRATCH_BYTES, PLAN_FIELDS, STATUS, TgemmError, library_path, load,
-    tgemm_attention_fwd, tgemm_last_device_status, tgemm_plan, tgemm_run, tgemm_run_ex, tgemm_run_host,
-    tgemm_run_noalloc,
+    EXPORTED, NOALLOC_SCRATCH_BYTES, PLAN_FIELDS, STATUS, TgemmError, library_path, load, load_debug,
+    tgemm_attention_fwd, tgemm_debug_last_check, tgemm_last_device_status, tgemm_plan, tgemm_run,
+    tgemm_run_ex, tgemm_run_host, tgemm_run_noalloc,
     tgemm_status_string, tgemm_version,
 )
 from .build import build  # noqa: F401

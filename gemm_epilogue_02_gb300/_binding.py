@@ -17,16 +17,17 @@ TGEMM_EPI_NONE, TGEMM_EPI_RELU, TGEMM_EPI_BIAS, TGEMM_EPI_BIAS_RELU = 0, 1, 2, 3
 TGEMM_EPI_GELU, TGEMM_EPI_BIAS_GELU = 4, 5
 STATUS = {0: "TGEMM_OK", 1: "TGEMM_ERR_INVALID_ARG", 2: "TGEMM_ERR_ALIGNMENT",
           3: "TGEMM_ERR_UNSUPPORTED_DEVICE", 4: "TGEMM_ERR_ALIAS", 5: "TGEMM_ERR_CUDA",
-          6: "TGEMM_ERR_TIMEOUT", 7: "TGEMM_ERR_SCRATCH_LIMIT"}
+          6: "TGEMM_ERR_TIMEOUT", 7: "TGEMM_ERR_SCRATCH_LIMIT", 8: "TGEMM_ERR_DEBUG_CHECK"}
 EXPORTED = ("tgemm_run", "tgemm_run_ex", "tgemm_run_host", "tgemm_status_string",
             "tgemm_last_device_status", "tgemm_version", "tgemm_run_noalloc", "tgemm_plan",
-            "tgemm_attention_fwd")
+            "tgemm_attention_fwd", "tgemm_debug_last_check")
 PLAN_FIELDS = ("bn", "cg", "stages", "tiles", "groups", "split_k", "split_first", "narrow_first",
                "narrow_parts", "units")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 _lock = threading.Lock()
 _lib = None
+_debug_lib = None
 
 
 class TgemmError(RuntimeError):
@@ -36,39 +37,61 @@ class TgemmError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The library load() uses: the debug build when TGEMM_DEBUG=1 is set."""
+    return _build.DEBUG_LIB if os.environ.get("TGEMM_DEBUG") == "1" else _build.LIB
+
+
+def _configure(lib: ctypes.CDLL) -> ctypes.CDLL:
+    p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    for name in ("tgemm_run", "tgemm_run_host", "tgemm_run_noalloc"):
+        f = getattr(lib, name)
+        f.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p]
+        f.restype = i32
+    lib.tgemm_run_ex.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, p]
+    lib.tgemm_run_ex.restype = i32
+    lib.tgemm_status_string.argtypes = [i32]
+    lib.tgemm_status_string.restype = ctypes.c_char_p
+    lib.tgemm_last_device_status.argtypes = []
+    lib.tgemm_last_device_status.restype = i32
+    lib.tgemm_debug_last_check.argtypes = []
+    lib.tgemm_debug_last_check.restype = i32
+    lib.tgemm_version.argtypes = []
+    lib.tgemm_version.restype = i32
+    lib.tgemm_plan.argtypes = [i64, i64, i64, i32, p]
+    lib.tgemm_plan.restype = i32
+    lib.tgemm_attention_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, i32, i32, p]
+    lib.tgemm_attention_fwd.restype = i32
+    return lib
 
 
 def load(build_if_missing: bool = True) -> ctypes.CDLL:
-    """Load libtgemm.so (building it with nvcc if it is missing or stale)."""
+    """Load libtgemm.so, or libtgemm_debug.so when TGEMM_DEBUG=1 is set at the
+    first call (building them with nvcc if missing or stale)."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
         if build_if_missing:
             _build.build()
-        if not os.path.exists(_build.LIB):
-            raise RuntimeError(f"CUDA library {_build.LIB} is missing; run build() first")
-        lib = ctypes.CDLL(_build.LIB)
-        p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-        for name in ("tgemm_run", "tgemm_run_host", "tgemm_run_noalloc"):
-            f = getattr(lib, name)
-            f.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p]
-            f.restype = i32
-        lib.tgemm_run_ex.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, p]
-        lib.tgemm_run_ex.restype = i32
-        lib.tgemm_status_string.argtypes = [i32]
-        lib.tgemm_status_string.restype = ctypes.c_char_p
-        lib.tgemm_last_device_status.argtypes = []
-        lib.tgemm_last_device_status.restype = i32
-        lib.tgemm_version.argtypes = []
-        lib.tgemm_version.restype = i32
-        lib.tgemm_plan.argtypes = [i64, i64, i64, i32, p]
-        lib.tgemm_plan.restype = i32
-        lib.tgemm_attention_fwd.argtypes = [p, p, p, p, i64, i64, i64, i64, i32, i32, p]
-        lib.tgemm_attention_fwd.restype = i32
-        _lib = lib
-        return lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is missing; run build() first")
+        _lib = _configure(ctypes.CDLL(path))
+        return _lib
+
+
+def load_debug(build_if_missing: bool = True) -> ctypes.CDLL:
+    """The debug build, loaded beside the library load() returns (its own
+    device state); for tests that run both on the same inputs."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            if build_if_missing:
+                _build.build()
+            if not os.path.exists(_build.DEBUG_LIB):
+                raise RuntimeError(f"CUDA library {_build.DEBUG_LIB} is missing; run build() first")
+            _debug_lib = _configure(ctypes.CDLL(_build.DEBUG_LIB))
+        return _debug_lib
 
 
 def tgemm_run(A: int, B: int, bias: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
@@ -112,6 +135,12 @@ def tgemm_status_string(status: int) -> str:
 
 def tgemm_last_device_status() -> int:
     return int(load().tgemm_last_device_status())
+
+
+def tgemm_debug_last_check() -> int:
+    """Id of the first failed device-side check of the debug build since the
+    last call (0: none; -1: the loaded library is the release build)."""
+    return int(load().tgemm_debug_last_check())
 
 
 def tgemm_version() -> int:

@@ -1,9 +1,11 @@
-"""Build step for the CUDA library: one nvcc invocation, sm_103a only, in-tree.
+"""Build step for the CUDA library: nvcc, sm_103a only, in-tree.
 
-Produces gemm_epilogue_02_gb300/libtgemm.so (git-ignored) from csrc/tgemm_api.cu.
-The CUDA runtime is linked statically and the driver's tensor-map encoder is
-looked up at run time, so the library loads (for symbol checks) on a host
-without a GPU driver.
+Produces gemm_epilogue_02_gb300/libtgemm.so (git-ignored) from
+csrc/tgemm_api.cu, and its debug build libtgemm_debug.so (-DTGEMM_DEBUG: the
+device-side bounds and alignment checks of csrc/debug_checks.cuh), the two
+compiled in parallel.  The CUDA runtime is linked statically and the
+driver's tensor-map encoder is looked up at run time, so the libraries load
+(for symbol checks) on a host without a GPU driver.
 """
 from __future__ import annotations
 
@@ -18,6 +20,7 @@ SRC = os.path.join(HERE, "csrc", "tgemm_api.cu")
 # Every header the translation unit includes: all of csrc/*.cuh and the C ABI.
 DEPS = sorted(glob.glob(os.path.join(HERE, "csrc", "*.cuh"))) + [os.path.join(ROOT, "include", "tgemm.h")]
 LIB = os.path.join(HERE, "libtgemm.so")
+DEBUG_LIB = os.path.join(HERE, "libtgemm_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -33,25 +36,36 @@ def command(out: str, extra=()) -> list:
             "-Xcompiler", "-fPIC", "-shared", "-cudart", "static", *extra, "-o", out, SRC]
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in [SRC, *DEPS])
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile libtgemm.so if missing or older than its sources; return its path."""
-    if not force and not stale():
-        return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = command(tmp, ["-Xptxas", "-v"] if verbose else [])
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
-    if verbose:
-        print(r.stdout + r.stderr)
-    os.replace(tmp, LIB)
+def _start(lib: str, verbose: bool):
+    tmp = lib + f".tmp{os.getpid()}"
+    extra = (["-DTGEMM_DEBUG"] if lib == DEBUG_LIB else []) + (["-Xptxas", "-v"] if verbose else [])
+    cmd = command(tmp, extra)
+    return lib, tmp, cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+
+
+def build(force: bool = False, verbose: bool = False, debug: bool = True) -> str:
+    """Compile libtgemm.so (and, with debug, libtgemm_debug.so) if missing or
+    older than the sources, in parallel; return the release library's path."""
+    libs = [LIB] + ([DEBUG_LIB] if debug else [])
+    jobs = [_start(lib, verbose) for lib in libs if force or stale(lib)]
+    errors = []
+    for lib, tmp, cmd, proc in jobs:
+        out, _ = proc.communicate()
+        if proc.returncode != 0:
+            errors.append("nvcc failed:\n" + " ".join(cmd) + "\n" + out)
+            continue
+        if verbose:
+            print(out)
+        os.replace(tmp, lib)
+    if errors:
+        raise RuntimeError("\n".join(errors))
     return LIB
 
 

@@ -51,6 +51,7 @@ struct AttnParams {
     float scale_log2;                 // log2(e) / sqrt(dim)
     void *O;
     unsigned int *status;
+    long long dbg_o_elems;            // debug builds: O's elements (B * S * H * dim)
 #ifdef TGEMM_TRACE
     unsigned long long *trace;        // trace builds: per-block cycle stamps of the first CTA
 #endif
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     uint8_t *smem = smem_raw;
     const uint32_t sbase = smem_u32(smem);
     if (sbase & 1023u) {
-        if (threadIdx.x == 0) atomicExch(p.status, kStatusLaunch);
+        if (threadIdx.x == 0) record_status(p.status, kStatusLaunch);
         return;
     }
     // Causal tiles near the end of the sequence have the most key blocks: they
@@ -388,10 +389,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             tmem_ld_32x32b_x32(lane_base + L::kColO + 32u, o[1]);
             tmem_wait_ld(o[0]);
             tmem_wait_ld(o[1]);
-            if (query < p.S) {
+            const long long o_off = ((static_cast<long long>(b) * p.S + query) * p.H + h) * kAttnD;
+            if (query < p.S && TGEMM_CHECK(o_off >= 0 && o_off + kAttnD <= p.dbg_o_elems, kChkAttnStore, p.status)) {
                 const float inv = 1.0f / l;
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<unsigned short *>(p.O) +
-                                                       ((static_cast<long long>(b) * p.S + query) * p.H + h) * kAttnD);
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<unsigned short *>(p.O) + o_off);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const int c = q / 4, i0 = (q % 4) * 8;

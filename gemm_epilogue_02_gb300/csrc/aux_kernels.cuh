@@ -5,6 +5,7 @@
 #include <cstdint>
 
 #include "bytes.cuh"
+#include "debug_checks.cuh"
 #include "ptx.cuh"
 
 namespace tgemm {
@@ -35,9 +36,11 @@ __device__ __forceinline__ uint4 load_block16(const unsigned char *__restrict__ 
 // destination row (8 elements) from the two aligned 16-byte source blocks it
 // straddles, shifted by o bytes.  The destination's pitch padding of the last
 // vector is written as zero.  HBM-bound: 2 x rows x cols x 2 bytes.
+// dst_elems (rows x ldd) and status serve the debug build's store check.
 __global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t *__restrict__ src, long long lds,
                                                           uint16_t *__restrict__ dst, long long ldd,
-                                                          long long rows, long long cols) {
+                                                          long long rows, long long cols, long long dst_elems,
+                                                          unsigned int *status) {
     // The fused kernel that reads dst may launch (and set itself up) now; it
     // waits for this grid's completion before its first global access.
     griddep_launch_dependents();
@@ -64,7 +67,7 @@ __global__ void __launch_bounds__(256) repack_rows_kernel(const uint16_t *__rest
                 }
                 out = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            d[v] = out;
+            if (TGEMM_CHECK(r * ldd + 8 * v + 8 <= dst_elems, kChkRepack, status)) d[v] = out;
         }
     }
 }

@@ -54,6 +54,7 @@
 
 #include <type_traits>
 
+#include "debug_checks.cuh"
 #include "ptx.cuh"
 
 namespace tgemm {
@@ -112,6 +113,10 @@ struct KParams {
     uint32_t test_extra_tx;
     uint32_t idesc;
     unsigned int *status;      // device status word
+    // Bounds of the debug build's checks (debug_checks.cuh), from the host's
+    // allocation sizes: C's elements from C (row-major, pitch ldc), the
+    // split-K scratch in floats, the arrival counters in words.
+    long long dbg_c_elems, dbg_partial_floats, dbg_counter_words;
 #ifdef TGEMM_TRACE
     unsigned long long *trace; // timeline stamps of the first CTAs (trace builds only)
 #endif
@@ -215,7 +220,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 *abort_flag = 1;
-                atomicExch(status, kStatusTimeout);
+                record_status(status, kStatusTimeout);
                 return false;
             }
         }
@@ -382,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Swizzled TMA tiles need a 1 KiB-aligned base.  The same for every CTA, so
     // all threads (and both CTAs of a pair) leave together before any barrier.
     if ((sbase & 1023u) || (MODE >= 0 && (p.is_bf16 ? 3 : 0) + p.act != MODE)) {
-        if (threadIdx.x == 0) atomicExch(p.status, kStatusLaunch);
+        if (threadIdx.x == 0) record_status(p.status, kStatusLaunch);
         return;
     }
     const uint32_t bar0 = sbase + L::kOffBar;
@@ -485,7 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = w.kb0; kb < w.kb1; kb += KSUB) {
                     const int nkb = min(KSUB, w.kb1 - kb);
                     const uint32_t fb = (CG == 1) ? full_bar(fbar) : leader_full(fbar);
-                    auto load = [&](uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y) {
+                    // (Debug builds: a copy whose innermost coordinate is not 16-byte
+                    // aligned is recorded and skipped.)
+                    auto load = [&](uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y, uint32_t chk) {
+                        if (!TGEMM_CHECK((x & 7) == 0, chk, p.status)) return;
                         if constexpr (CG == 1) tma_load_2d(dst, m, fb, x, y);
                         else tma_load_2d_pair(dst, m, fb, x, y);
                     };
@@ -514,12 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t b_dst = sbase + L::kOffB + stage * L::kBBytes;
                         if (!p.a_mn) {
                             // A [M, K]: one box of 128 rows x 64 k (K-major, 128-byte rows).
-                            load(a_dst, &tmA, k0, a_row);
+                            load(a_dst, &tmA, k0, a_row, kChkTmaLoadA);
                         } else {
                             // A stored [K, M]: two boxes of 64 k-rows x 64 m (MN-major).
 #pragma unroll
                             for (int j = 0; j < kBM / 64; ++j)
-                                load(a_dst + j * (kBK * 128), &tmA, a_row + j * 64, k0);
+                                load(a_dst + j * (kBK * 128), &tmA, a_row + j * 64, k0, kChkTmaLoadA);
                         }
                         if (MC == 2 && !narrow) {
                             // This CTA's B slice is shared with the same rank of the other
@@ -527,10 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // [N, K], 64-row) sub-tiles and multicasts it to both.
                             const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (CG + rank)));
                             const int sub0 = b_col + static_cast<int>(pp) * 64;
-                            if (!p.b_kmajor)
-                                tma_load_2d_pair_mc(b_dst + pp * (kBK * 128), p.b_3d ? &tmB2 : &tmB, fb, sub0, k0, mask);
-                            else
+                            if (!p.b_kmajor) {
+                                if (TGEMM_CHECK((sub0 & 7) == 0, kChkTmaLoadB, p.status))
+                                    tma_load_2d_pair_mc(b_dst + pp * (kBK * 128), p.b_3d ? &tmB2 : &tmB, fb, sub0, k0, mask);
+                            } else if (TGEMM_CHECK((k0 & 7) == 0, kChkTmaLoadB, p.status)) {
                                 tma_load_2d_pair_mc(b_dst + pp * (64 * 128), &tmB2, fb, k0, sub0, mask);
+                            }
                         } else if (p.b_3d && !narrow) {
                             // B [K, N] viewed as (64 columns, K rows, column chunks): one box
                             // holds the kBSub 64-column sub-tiles of 64 k-rows (MN-major),
@@ -543,11 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const CUtensorMap *mb = p.b_3d ? &tmB2 : &tmB;
 #pragma unroll
                             for (int j = 0; j < L::kBSub; ++j)
-                                if (j < b_sub) load(b_dst + j * (kBK * 128), mb, b_col + j * 64, k0);
+                                if (j < b_sub) load(b_dst + j * (kBK * 128), mb, b_col + j * 64, k0, kChkTmaLoadB);
                         } else {
                             // B stored [N, K]: one box of BN/CG n-rows x 64 k (K-major); a
                             // narrow unit's MMA reads only the first width / CG of them.
-                            load(b_dst, &tmB, k0, b_col);
+                            load(b_dst, &tmB, k0, b_col, kChkTmaLoadB);
                         }
                         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                     }
@@ -708,9 +718,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool has_next = u + num_groups < p.num_units;
             int next_cb = 0, next_wd = 0;
             if (has_next) unit_cols(u + num_groups, next_cb, next_wd);
-            if (split >= 0 && lane == 0)
-                atomicMax(p.counters + (t - p.split_first) * (kCluster * kEpiWarps) + static_cast<int>(crank) * kEpiWarps + ew,
-                          p.epoch << 16);
+            if (split >= 0 && lane == 0) {
+                const long long ci = static_cast<long long>(t - p.split_first) * (kCluster * kEpiWarps) +
+                                     static_cast<int>(crank) * kEpiWarps + ew;
+                if (TGEMM_CHECK(ci >= 0 && ci < p.dbg_counter_words, kChkCounter, p.status))
+                    atomicMax(p.counters + ci, p.epoch << 16);
+            }
             int ok = 1;
             if (lane == 0) ok = wait_bar<true>(tfull_bar(acc), acc_phase, abort_flag, p.status) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -795,7 +808,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmC, sb, n0, m0);
+                        if (TGEMM_CHECK(n0 >= 0 && (n0 & 7) == 0 && m0 >= 0 &&
+                                            static_cast<long long>(m0) * p.ldc < p.dbg_c_elems,
+                                        kChkTmaStoreC, p.status))
+                            tma_store_2d(&tmC, sb, n0, m0);
                         bulk_commit_group();
                     }
                 } else {
@@ -813,7 +829,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (row >= p.M) break;
                             const uint32_t v = *reinterpret_cast<const uint32_t *>(
                                 sb_gen + rr * kRowBytes + ((((lane >> 2) ^ swz(rr)) << 4) | ((lane & 3) << 2)));
-                            unsigned short *dst = Cg + static_cast<long long>(row) * p.ldc + col;
+                            const long long off = static_cast<long long>(row) * p.ldc + col;
+                            unsigned short *dst = Cg + off;
+                            if (!TGEMM_CHECK(col >= p.N || off + (col + 1 < p.N ? 1 : 0) < p.dbg_c_elems, kChkStoreC,
+                                             p.status))
+                                continue;
                             if (col < p.N) dst[0] = static_cast<unsigned short>(v & 0xFFFFu);
                             if (col + 1 < p.N) dst[1] = static_cast<unsigned short>(v >> 16);
                         }
@@ -845,6 +865,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // This range's fp32 partials, TMEM loads double-buffered (the first
                     // one went out at the unit's start).
                     auto write_partial = [&](int sub, const uint32_t (&r)[32]) {
+                        if (!TGEMM_CHECK((mine - p.partials) + (sub + 1) * 1024ll <= p.dbg_partial_floats,
+                                         kChkPartial, p.status))
+                            return;
 #pragma unroll
                         for (int g = 0; g < 8; ++g)
                             __stcg(reinterpret_cast<float4 *>(mine + sub * 1024 + g * 128 + lane * 4),
@@ -868,9 +891,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (warp == 2 && lane == 0 && tile_i == 0) TGEMM_STAMP(41);
                     unsigned int arrived = 0;
-                    if (lane == 0)   // the word is at least epoch << 16 already (raised at the unit's start)
-                        arrived = static_cast<unsigned int>(
-                            atomicAdd(p.counters + ts * (kCluster * kEpiWarps) + wid, 1ull) - (p.epoch << 16));
+                    const long long ci = static_cast<long long>(ts) * (kCluster * kEpiWarps) + wid;
+                    if (lane == 0 && TGEMM_CHECK(ci < p.dbg_counter_words, kChkCounter, p.status))
+                        // the word is at least epoch << 16 already (raised at the unit's start)
+                        arrived = static_cast<unsigned int>(atomicAdd(p.counters + ci, 1ull) - (p.epoch << 16));
                     arrived = __shfl_sync(0xffffffffu, arrived, 0);
 #ifdef TGEMM_TRACE
                     if (warp == 2 && lane == 0 && tile_i == 0 && blockIdx.x < 160) {
@@ -896,6 +920,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const bool two = kStep == 2 && rg + 1 < p.split_k;
                                 const float *src0 = region(rg) + sub * 1024 + lane * 4;
                                 const float *src1 = region(two ? rg + 1 : rg) + sub * 1024 + lane * 4;
+                                if (!TGEMM_CHECK((region(two ? rg + 1 : rg) - p.partials) + (sub + 1) * 1024ll <=
+                                                     p.dbg_partial_floats,
+                                                 kChkPartial, p.status))
+                                    continue;
                                 float4 v0[8], v1[8];
 #pragma unroll
                                 for (int g = 0; g < 8; ++g) {

@@ -503,13 +503,25 @@ cudaError_t launch_config(DeviceInfo *d, const Cfg &cfg, const CUtensorMap &ta, 
 }
 
 cudaError_t repack(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t rows, int64_t cols,
-                   cudaStream_t s) {
+                   unsigned int *status, cudaStream_t s) {
     const dim3 block(256);
     const dim3 grid(static_cast<unsigned>(std::min<int64_t>(cdiv(cdiv(cols, 8), 256), 64)),
                     static_cast<unsigned>(std::min<int64_t>(rows, 65535)));
     repack_rows_kernel<<<grid, block, 0, s>>>(static_cast<const uint16_t *>(src), lds,
-                                              static_cast<uint16_t *>(dst), ldd, rows, cols);
+                                              static_cast<uint16_t *>(dst), ldd, rows, cols, rows * ldd, status);
     return cudaGetLastError();
+}
+
+// Debug builds: the bound of the checks on C's elements, (M - 1) * ldc + N.
+// Testing only: TGEMM_DEBUG_PLANT=c_store moves it one row up, so that the
+// checks refuse (and skip) every plain store of C's last row.
+long long debug_c_bound(int64_t M, int64_t N, int64_t ldc) {
+    long long e = (M - 1) * ldc + N;
+#ifdef TGEMM_DEBUG
+    if (const char *v = std::getenv("TGEMM_DEBUG_PLANT"))
+        if (std::string(v) == "c_store") e -= ldc;
+#endif
+    return e;
 }
 
 // Tensor maps of A, B (for their stored layouts, 16-byte pitches) and C for
@@ -635,7 +647,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
         lda_use = cdiv(a_cols, 8) * 8;
         if (cudaMallocFromPoolAsync(&scratch_a, static_cast<size_t>(a_rows * lda_use * 2), d->pool,
                                     stream) != cudaSuccess ||
-            repack(A, lda, scratch_a, lda_use, a_rows, a_cols, stream) != cudaSuccess)
+            repack(A, lda, scratch_a, lda_use, a_rows, a_cols, d->status, stream) != cudaSuccess)
             st = TGEMM_ERR_CUDA;
         a_use = scratch_a;
     }
@@ -643,7 +655,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
         ldb_use = cdiv(b_cols, 8) * 8;
         if (cudaMallocFromPoolAsync(&scratch_b, static_cast<size_t>(b_rows * ldb_use * 2), d->pool,
                                     stream) != cudaSuccess ||
-            repack(B, ldb, scratch_b, ldb_use, b_rows, b_cols, stream) != cudaSuccess)
+            repack(B, ldb, scratch_b, ldb_use, b_rows, b_cols, d->status, stream) != cudaSuccess)
             st = TGEMM_ERR_CUDA;
         b_use = scratch_b;
     }
@@ -674,6 +686,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
+    p.dbg_c_elems = debug_c_bound(M, N, ldc);
 #ifdef TGEMM_TRACE
     p.trace = g_trace_buffer;
 #endif
@@ -705,6 +718,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
             return TGEMM_ERR_CUDA;
         }
         p.partials = static_cast<float *>(scratch_split);
+        p.dbg_partial_floats = pbytes / 4;
         // The stream's arrival counters: zeroed once when (re)allocated, then
         // told apart between launches by the epoch (no clearing per call, so
         // nothing is enqueued between the previous kernel and this one).
@@ -732,6 +746,7 @@ tgemm_status run_device(DeviceInfo *d, const void *A, const void *B, const void 
                 cb.bytes = want;
             }
             p.counters = static_cast<unsigned long long *>(cb.ptr);
+            p.dbg_counter_words = static_cast<long long>(cb.bytes / sizeof(unsigned long long));
             p.epoch = d->epoch;
         }
     }
@@ -828,14 +843,14 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
     if (used > static_cast<int64_t>(kNoAllocScratchBytes)) return TGEMM_ERR_SCRATCH_LIMIT;
     unsigned char *scratch = static_cast<unsigned char *>(nd->scratch);
     if (a_off >= 0) {
-        if (repack(A, lda, scratch + a_off, lda_use, M, K, stream) != cudaSuccess) {
+        if (repack(A, lda, scratch + a_off, lda_use, M, K, d->status, stream) != cudaSuccess) {
             cudaGetLastError();
             return TGEMM_ERR_CUDA;
         }
         a_use = scratch + a_off;
     }
     if (b_off >= 0) {
-        if (repack(B, ldb, scratch + b_off, ldb_use, K, N, stream) != cudaSuccess) {
+        if (repack(B, ldb, scratch + b_off, ldb_use, K, N, d->status, stream) != cudaSuccess) {
             cudaGetLastError();
             return TGEMM_ERR_CUDA;
         }
@@ -861,6 +876,7 @@ tgemm_status run_device_noalloc(NoAllocDevice *nd, const void *A, const void *B,
     p.is_bf16 = bf16 ? 1 : 0;
     p.tma_store = tma_store ? 1 : 0;
     p.status = d->status;
+    p.dbg_c_elems = debug_c_bound(M, N, ldc);
     // No split-K here (its partials would need scratch); the narrow tail needs none.
     const Plan plan = choose_plan(cfg, M, N, K, d->num_sms, false);
     p.narrow_first = static_cast<int>(plan.narrow_first);
@@ -1011,6 +1027,7 @@ extern "C" tgemm_status tgemm_attention_fwd(const void *Q, const void *K, const 
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(dim)));
     p.O = O;
     p.status = d->status;
+    p.dbg_o_elems = rows * dim;
 #ifdef TGEMM_TRACE
     p.trace = g_trace_buffer;
 #endif
@@ -1185,6 +1202,7 @@ extern "C" const char *tgemm_status_string(tgemm_status s) {
         case TGEMM_ERR_CUDA: return "TGEMM_ERR_CUDA: a CUDA call or launch failed";
         case TGEMM_ERR_TIMEOUT: return "TGEMM_ERR_TIMEOUT: a kernel gave up on a pipeline wait";
         case TGEMM_ERR_SCRATCH_LIMIT: return "TGEMM_ERR_SCRATCH_LIMIT: repacked operands exceed the fixed scratch of tgemm_run_noalloc";
+        case TGEMM_ERR_DEBUG_CHECK: return "TGEMM_ERR_DEBUG_CHECK: a device-side check of the debug build failed (access skipped)";
     }
     return "TGEMM_ERR_UNKNOWN";
 }
@@ -1204,6 +1222,26 @@ extern "C" tgemm_status tgemm_last_device_status(void) {
         return TGEMM_ERR_CUDA;
     }
     return v ? static_cast<tgemm_status>(v) : TGEMM_OK;
+}
+
+extern "C" int tgemm_debug_last_check(void) {
+#ifdef TGEMM_DEBUG
+    DeviceInfo *d = nullptr;
+    if (current_device(&d) != TGEMM_OK) return 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_debug_check, sizeof(v)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_debug_check, &zero, sizeof(zero)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return static_cast<int>(v);
+#else
+    return -1;
+#endif
 }
 
 extern "C" int tgemm_version(void) { return kVersion; }

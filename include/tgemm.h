@@ -60,7 +60,9 @@ typedef enum {
     TGEMM_ERR_ALIAS = 4,              /* C's byte range overlaps A, B or bias                */
     TGEMM_ERR_CUDA = 5,               /* a CUDA runtime/driver call or a launch failed       */
     TGEMM_ERR_TIMEOUT = 6,            /* a kernel gave up on a pipeline wait (device status) */
-    TGEMM_ERR_SCRATCH_LIMIT = 7       /* tgemm_run_noalloc: repacked operands exceed its fixed scratch */
+    TGEMM_ERR_SCRATCH_LIMIT = 7,      /* tgemm_run_noalloc: repacked operands exceed its fixed scratch */
+    TGEMM_ERR_DEBUG_CHECK = 8         /* debug build: a device-side bounds / alignment check failed
+                                         and the access was skipped (device status) */
 } tgemm_status;
 
 /*
@@ -222,10 +224,32 @@ const char *tgemm_status_string(tgemm_status status);
  * tgemm_last_device_status — read and clear the device-side status word of the
  * current device.  Kernels bound every pipeline wait by a time limit; a wait
  * that runs out records TGEMM_ERR_TIMEOUT here and the kernel returns early
- * (its output is then invalid).  Synchronises the device.  Returns TGEMM_OK
- * when no kernel has timed out since the last call.
+ * (its output is then invalid).  In the debug build a failed device-side check
+ * records TGEMM_ERR_DEBUG_CHECK, and the first error since the last call is
+ * kept (the release build keeps the last).  Synchronises the device.  Returns TGEMM_OK when no kernel has reported an
+ * error since the last call.
  */
 tgemm_status tgemm_last_device_status(void);
+
+/*
+ * tgemm_debug_last_check — the debug build (libtgemm_debug.so, compiled with
+ * -DTGEMM_DEBUG; the Python binding loads it when TGEMM_DEBUG=1 is set): the
+ * id of the first device-side check that failed since the last call, then
+ * cleared; 0 when none failed.  The checks guard the error classes the
+ * TileLang tutorial names for hand-written kernels: 1 / 2 a TMA load of A /
+ * B whose innermost coordinate is not 16-byte aligned, 3 a TMA store of C
+ * starting at a negative, unaligned or out-of-range coordinate, 4 a plain
+ * store of C outside its (M - 1) * ldc + N elements, 5 a split-K partial
+ * outside its scratch, 6 an arrival counter outside its buffer, 7 an
+ * attention output store outside O, 8 a repack store outside its
+ * destination.  The failing access is skipped (nothing traps); a skipped
+ * copy leaves its pipeline slot incomplete, which the bounded waits end.
+ * Synchronises the device.  Returns -1 in the release build, which compiles
+ * no checks.  Testing only: TGEMM_DEBUG_PLANT=c_store makes the debug build's
+ * bound for C one row short, so that check 4 fires on C's last row (whose
+ * stores are then skipped).
+ */
+int tgemm_debug_last_check(void);
 
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int tgemm_version(void);

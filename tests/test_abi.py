@@ -34,6 +34,17 @@ def test_library_exports_every_declared_symbol():
     assert tg.tgemm_version() == 0x000100
 
 
+def test_debug_build_exports_the_same_abi():
+    """libtgemm_debug.so (the device-side checks compiled in) has the same
+    C ABI; the release build says it compiles no checks."""
+    dbg = tg.load_debug()
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    assert dbg.tgemm_version() == tg.tgemm_version()
+    assert tg.load().tgemm_debug_last_check() == -1   # release build: no checks, no device access
+    assert dbg.tgemm_status_string(8).decode().startswith("TGEMM_ERR_DEBUG_CHECK")
+
+
 def test_header_documents_every_environment_variable_the_library_reads():
     src_dir = os.path.join(ROOT, "gemm_epilogue_02_gb300", "csrc")
     names = set()
