@@ -60,7 +60,8 @@ struct AttnParams {
 // Trace builds only: clock64 stamps of the first CTA (blockIdx 0,0,0):
 // p.trace[kind * 32 + j] for key block j < 32; kind 0 softmax past the score
 // wait, 1 scores read, 2 exponentials done, 3 past the P.V wait, 4 P published
-// (softmax warp 4 lane 0); 5 MMA lane past the P wait, 6 P.V issued.
+// (softmax warp 4 lane 0); 5 MMA lane past the P wait, 6 P.V issued, 7 MMA
+// lane past the K/V wait, 8 past the score-buffer wait (S_j issued next).
 #ifdef TGEMM_TRACE
 #define ATTN_STAMP(kind, j)                                                                   \
     do {                                                                                      \
@@ -227,11 +228,16 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     // The score buffer is free once the softmax has read S_{j-1}.
                     const int s = j % kAttnStages;
                     if (!wait_bar<false>(kv_full(s), static_cast<uint32_t>(j / kAttnStages) & 1u, abort_flag,
-                                         p.status) ||
-                        !wait_bar<true>(s_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, abort_flag, p.status)) {
+                                         p.status)) {
                         ok = false;
                         break;
                     }
+                    ATTN_STAMP(7, j);
+                    if (!wait_bar<true>(s_empty, (static_cast<uint32_t>(j) & 1u) ^ 1u, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    ATTN_STAMP(8, j);
                     tc_fence_after();
                     const uint64_t k_desc = sw128_desc(sbase + L::kKV + s * 2 * L::kTile, 16, 1024);
                     if (issuer) {
